@@ -1,0 +1,518 @@
+"""Benchmark: one decode step of paged attention over a block-tabled KV cache.
+
+A step is the whole decode hot path on one batch: write each sequence's fresh
+token K/V into its cache slot (pa_reshape_and_cache), then decode attention
+(pa_decode: split-K pass + log-sum-exp reduce).  The default workload is the
+long-context decode batch: 8 sequences with cached lengths uniform in
+[16384, 32768], block size 32, 32 query / 8 kv heads, head dim 128, bf16 cache
+(about 0.8 GB of K/V read per step, larger than L2; L2 is also flushed
+between timed steps).
+
+Prints ONE JSON line (rank 0).  ``value`` is achieved HBM GB/s of the step:
+algorithmic bytes (every visible K/V element read once, q read, output and
+fresh K/V written, block-table entries read) over the device time of the step.
+``--impl reference`` times the fp64 CPU oracle on the same workload instead.
+Multi-GPU (torchrun): every rank runs its own replica (weak scaling, no
+data-path collective); the step time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+from pathlib import Path
+
+import torch
+
+ROOT = Path(__file__).resolve().parent
+sys.path.insert(0, str(ROOT))
+
+import workloads  # noqa: E402
+
+METRIC = "paged-attn decode achieved HBM GB/s (% of GB300 peak) and seq-steps/s"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+NOMINAL_HBM_GBS = 8000.0
+
+
+# ----------------------------------------------------------------------------- helpers
+
+def peaks():
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        d = json.loads(p.read_text())
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def decode_bytes(case) -> dict:
+    """Algorithmic bytes of one decode step (each visible K/V element read once)."""
+    eb = case.kv_elem_bytes()
+    S, Hq, Hkv, D, bs = case.num_seqs, case.num_heads, case.num_kv_heads, case.head_dim, case.block_size
+    ctx = case.context_lens.to(torch.int64)
+    kv = int(ctx.sum()) * Hkv * D * eb * 2
+    q = S * Hq * D * eb
+    out = S * Hq * D * 4
+    tables = int(((ctx + bs - 1) // bs).sum()) * 4 + S * 4
+    fresh = case.new_key.numel() * eb * 2 * 2 + case.slot_mapping.numel() * 8  # read + write
+    return {"kv": kv, "decode": kv + q + out + tables, "step": kv + q + out + tables + fresh}
+
+
+def prefill_work(case) -> tuple[float, int]:
+    """Causal-exact FLOPs (QK^T and PV) and algorithmic bytes of one prefill call."""
+    eb = case.kv_elem_bytes()
+    Hq, Hkv, D = case.num_heads, case.num_kv_heads, case.head_dim
+    qsl = case.query_start_loc.tolist()
+    pairs = 0
+    for s in range(case.num_seqs):
+        lq, c = qsl[s + 1] - qsl[s], int(case.context_lens[s])
+        pairs += sum(c - lq + i + 1 for i in range(lq))
+    flops = 4.0 * D * Hq * pairs
+    byts = int(case.context_lens.sum()) * Hkv * D * eb * 2 + case.query.numel() * eb + case.query.numel() * 4
+    return flops, byts
+
+
+def kernel_source_hash() -> str:
+    src = (ROOT / "paged_kv_attention_write_gb300" / "csrc" / "decode.cu").read_bytes()
+    return hashlib.sha256(src).hexdigest()[:16]
+
+
+def profiled_traffic():
+    """DRAM bytes per decode launch from the committed ncu summary, if it was taken on the
+    current decode kernel source; else None."""
+    p = ROOT / "profiles" / "traffic.json"
+    if not p.exists():
+        return None
+    d = json.loads(p.read_text())
+    e = d.get("decode")
+    if not e or e.get("source_sha256_16") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 100 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+class DecodeStep:
+    """Device-resident inputs of one decode step and the calls that run it."""
+
+    def __init__(self, case, device):
+        import paged_kv_attention_write_gb300 as pa
+        self.pa = pa
+        self.case = case
+        self.dev = device
+        self.kc = case.key_cache.to(device)
+        self.vc = case.value_cache.to(device)
+        self.bt = case.block_tables.to(device)
+        self.cl = case.context_lens.to(device)
+        self.q = case.query.to(device)
+        self.nk = case.new_key.to(device)
+        self.nv = case.new_value.to(device)
+        self.slots = case.slot_mapping.to(device)
+        self.out = torch.empty(tuple(case.query.shape), dtype=torch.float32, device=device)
+        nbytes = pa.pa_decode_workspace_size(case.num_seqs, case.num_heads, case.head_dim,
+                                             case.max_context_len)
+        self.ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=device)
+        self.max_ctx = case.max_context_len
+        # pinned host staging for the end-to-end measurement
+        self.h_in = {k: getattr(self, k).cpu().pin_memory() for k in ("q", "nk", "nv", "slots", "bt", "cl")}
+        self.h_out = torch.empty(self.out.shape, dtype=torch.float32).pin_memory()
+
+    def reshape(self):
+        self.pa.pa_reshape_and_cache(self.nk, self.nv, self.kc, self.vc, self.slots)
+
+    def decode(self):
+        self.pa.pa_decode(self.out, self.q, self.kc, self.vc, self.bt, self.cl, self.max_ctx,
+                          self.case.scale, workspace=self.ws)
+
+    def step(self):
+        self.reshape()
+        self.decode()
+
+    def e2e_step(self):
+        """Host buffers in, host result out: H2D of the step inputs, the step, D2H."""
+        for k, h in self.h_in.items():
+            getattr(self, k).copy_(h, non_blocking=True)
+        self.step()
+        self.h_out.copy_(self.out, non_blocking=True)
+
+    def h2d_bytes(self):
+        return sum(t.numel() * t.element_size() for t in self.h_in.values())
+
+    def d2h_bytes(self):
+        return self.h_out.numel() * self.h_out.element_size()
+
+    def launches_per_step(self):
+        np_ = math.ceil(self.max_ctx / 512)
+        return 2 + (1 if np_ > 1 else 0)
+
+
+def _barrier(dist_on):
+    if dist_on:
+        torch.distributed.barrier()
+
+
+def _max_over_ranks(x: float, dist_on: bool) -> float:
+    if not dist_on:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def time_steps(fn, steps, flush, dist_on):
+    """Per-step device time (ms) with CUDA events on the launching stream; L2 flushed before
+    each step outside the event pair.  The region is bracketed by barrier + synchronize."""
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    _barrier(dist_on)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(steps):
+        flush.zero_()
+        starts[i].record()
+        fn()
+        ends[i].record()
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    _barrier(dist_on)
+    ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    return ms, wall
+
+
+def gpu_arm(args, rank, world, dist_on):
+    device = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(device)
+    hbm_peak, tc_peak, peak_kind = peaks()
+    case = workloads.WORKLOADS[args.workload]()
+    if not case.is_decode:
+        raise SystemExit("the headline bench times a decode workload")
+    st = DecodeStep(case, device)
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=device)
+    byts = decode_bytes(case)
+
+    for _ in range(args.warmup):
+        st.step()
+    torch.cuda.synchronize()
+
+    # decode kernel alone (the dominant launch: split-K pass + reduce), then the whole step
+    dec_ms, _ = time_steps(st.decode, args.steps, flush, dist_on)
+    with ClockSampler(device.index) as clocks:
+        step_ms, wall = time_steps(st.step, args.steps, flush, dist_on)
+    for _ in range(3):
+        st.e2e_step()
+    torch.cuda.synchronize()
+    e2e_ms, _ = time_steps(st.e2e_step, max(3, args.steps // 4), flush, dist_on)
+
+    ms_step = _max_over_ranks(statistics.mean(step_ms), dist_on)
+    ms_dec = _max_over_ranks(statistics.mean(dec_ms), dist_on)
+    ms_e2e = _max_over_ranks(statistics.mean(e2e_ms), dist_on)
+    value = world * byts["step"] / (ms_step * 1e-3) / 1e9
+    dec_gbs = byts["decode"] / (ms_dec * 1e-3) / 1e9
+    e2e_gbs = world * byts["step"] / (ms_e2e * 1e-3) / 1e9
+
+    secondary = {}
+    if not args.no_secondary and rank == 0:
+        secondary = secondary_measurements(device, flush, hbm_peak, tc_peak, peak_kind)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(case, byts)
+
+    if rank != 0:
+        return None
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) q/k/v, shuffled block pool)",
+        "config": {
+            "workload": case.name,
+            "num_seqs": case.num_seqs,
+            "context_lens": case.context_lens.tolist(),
+            "block_size": case.block_size,
+            "num_heads": case.num_heads,
+            "num_kv_heads": case.num_kv_heads,
+            "head_dim": case.head_dim,
+            "kv_bytes_per_step": byts["kv"],
+            "l2": "inputs (0.8 GB of K/V) larger than L2, and L2 flushed (256 MB write) before each timed step",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+        },
+        "seq_steps_per_s": round(world * case.num_seqs / (ms_step * 1e-3), 1),
+        "pct_of_peak": {"measured_hbm": round(100 * value / world / hbm_peak, 1),
+                        "nominal_8TBs": round(100 * value / world / NOMINAL_HBM_GBS, 1)},
+        "roofline": {
+            "kernel": "pa_decode (split-K pass + log-sum-exp reduce)",
+            "bound": "hbm",
+            "achieved": round(dec_gbs, 1),
+            "peak": hbm_peak,
+            "unit": "GB/s",
+            "frac": round(dec_gbs / hbm_peak, 4),
+            "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback",
+            "traffic": profiled_traffic(),
+            "algorithmic_bytes_per_launch": byts["decode"],
+            "ms_per_launch": round(ms_dec, 5),
+        },
+        "e2e": {"value": round(e2e_gbs, 2), "unit": "GB/s", "ms_per_step": round(ms_e2e, 5),
+                "h2d_bytes_per_step": st.h2d_bytes(), "d2h_bytes_per_step": st.d2h_bytes()},
+        "gpu_launches": args.steps * st.launches_per_step(),
+        "clocks": clocks.summary(),
+        "timed_region_s": round(wall, 3),
+    }
+    if secondary:
+        line["secondary"] = secondary
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
+    return line
+
+
+def secondary_measurements(device, flush, hbm_peak, tc_peak, peak_kind):
+    """Shorter timings of the other hot-path rows: decode batch, chunked prefill, block copy."""
+    import paged_kv_attention_write_gb300 as pa
+    res = {}
+    case = workloads.decode_batch()
+    st = DecodeStep(case, device)
+    for _ in range(5):
+        st.step()
+    ms, _ = time_steps(st.decode, 50, flush, False)
+    b = decode_bytes(case)["decode"]
+    t = statistics.mean(ms)
+    res["decode_batch"] = {"workload": case.name, "ms": round(t, 5),
+                           "GB/s": round(b / t / 1e6, 1), "frac_hbm": round(b / t / 1e6 / hbm_peak, 4),
+                           "seq_steps_per_s": round(case.num_seqs / t * 1e3, 1)}
+    del st
+    case = workloads.prefill_chunk()
+    kc, vc = case.key_cache.to(device), case.value_cache.to(device)
+    bt, cl = case.block_tables.to(device), case.context_lens.to(device)
+    q, qsl = case.query.to(device), case.query_start_loc.to(device)
+    nk, nv, sl = case.new_key.to(device), case.new_value.to(device), case.slot_mapping.to(device)
+    out = torch.empty(tuple(q.shape), dtype=torch.float32, device=device)
+    mq = int((case.query_start_loc[1:] - case.query_start_loc[:-1]).max())
+    pa.pa_reshape_and_cache(nk, nv, kc, vc, sl)
+
+    def prefill():
+        pa.pa_prefill_chunk(out, q, qsl, mq, kc, vc, bt, cl, case.max_context_len, case.scale)
+    for _ in range(5):
+        prefill()
+    ms, _ = time_steps(prefill, 50, flush, False)
+    t = statistics.mean(ms)
+    flops, byts = prefill_work(case)
+    tfs = flops / (t * 1e-3) / 1e12
+    res["prefill_chunk"] = {"workload": case.name, "ms": round(t, 5), "TFLOP/s": round(tfs, 1),
+                            "bound": "tensor", "peak_tflops": tc_peak,
+                            "frac_tensor": round(tfs / tc_peak, 4),
+                            "GB/s": round(byts / (t * 1e-3) / 1e9, 1),
+                            "tokens_per_s": round(int(q.shape[0]) / (t * 1e-3), 1)}
+
+    def reshape():
+        pa.pa_reshape_and_cache(nk, nv, kc, vc, sl)
+    ms, _ = time_steps(reshape, 50, flush, False)
+    t = statistics.mean(ms)
+    rb = nk.numel() * nk.element_size() * 4 + sl.numel() * 8
+    res["reshape_and_cache_2048_tokens"] = {"ms": round(t, 5), "GB/s": round(rb / (t * 1e-3) / 1e9, 1)}
+    del kc, vc
+    # block copy: 26 recipients' leading blocks of the stress workload (bs 16, bf16)
+    case = workloads.stress_decode(block_size=16, dtype=torch.bfloat16)
+    kc, vc = case.key_cache.to(device), case.value_cache.to(device)
+    bm = case.block_mapping.to(device)
+
+    def copy():
+        pa.pa_copy_blocks(kc, vc, bm)
+    for _ in range(3):
+        copy()
+    ms, _ = time_steps(copy, 50, flush, False)
+    t = statistics.mean(ms)
+    cb = int(bm.shape[0]) * case.block_size * case.num_kv_heads * case.head_dim * 2 * 2 * 2
+    res["copy_blocks_stress"] = {"pairs": int(bm.shape[0]), "ms": round(t, 5),
+                                 "GB/s": round(cb / (t * 1e-3) / 1e9, 1)}
+    return res
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+
+def _oracle_step(oracle, case, kc, vc):
+    oracle.reshape_and_cache(case.new_key, case.new_value, kc, vc, case.slot_mapping, case.block_size)
+    return oracle.paged_attention(case.query, case.query_start_loc, kc, vc, case.block_tables,
+                                  case.context_lens, case.scale)
+
+
+def cpu_baseline(case, byts, reps: int = 2):
+    """The fp64 oracle, as it stands, on the host cores: whole steps of the same workload."""
+    import oracle
+    oracle.build()
+    kc, vc = case.key_cache.clone(), case.value_cache.clone()
+    times = []
+    for _ in range(reps):
+        t0 = time.perf_counter()
+        _oracle_step(oracle, case, kc, vc)
+        times.append(time.perf_counter() - t0)
+    t = statistics.median(times)
+    return {"value": round(byts["step"] / t / 1e9, 4), "unit": "GB/s", "cores": oracle.num_threads(),
+            "kind": "oracle", "seconds_per_step": round(t, 3),
+            "sample": f"{reps} whole steps of the same workload ({case.num_seqs} sequences, all heads), median"}
+
+
+def reference_arm(args, rank, world, budget_s: float = 150.0):
+    """``--impl reference``: the fp64 CPU oracle timed on the host cores (rank 0 only).
+
+    Each step is a bounded sample of the workload -- the first sequence, all heads, its
+    context truncated to the first T tokens -- with T calibrated so that the whole
+    ``--warmup W --steps K`` run takes about ``budget_s`` seconds."""
+    if rank != 0:
+        return None
+    import oracle
+    oracle.build()
+    case = workloads.WORKLOADS[args.workload]()
+    kc, vc = case.key_cache.clone(), case.value_cache.clone()
+
+    def sample(tokens: int):
+        sub = workloads.PagedCase(**{**case.__dict__})
+        sub.query = case.query[:1]
+        sub.query_start_loc = case.query_start_loc[:2]
+        sub.block_tables = case.block_tables[:1]
+        sub.context_lens = torch.tensor([tokens], dtype=torch.int32)
+        sub.new_key, sub.new_value = case.new_key[:1], case.new_value[:1]
+        sub.slot_mapping = case.slot_mapping[:1]
+        return sub
+
+    full = int(case.context_lens[0])
+    probe = sample(min(full, 2048))
+    t0 = time.perf_counter()
+    _oracle_step(oracle, probe, kc, vc)
+    per_token = (time.perf_counter() - t0) / int(probe.context_lens[0])
+    target = budget_s / (args.steps + args.warmup)
+    tokens = int(max(64, min(full, target / max(per_token, 1e-9))))
+    sub = sample(tokens)
+    sb = decode_bytes(sub)
+    for _ in range(args.warmup):
+        _oracle_step(oracle, sub, kc, vc)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        _oracle_step(oracle, sub, kc, vc)
+        times.append(time.perf_counter() - t0)
+    t = statistics.mean(times)
+    value = sb["step"] / t / 1e9
+    desc = (f"first sequence of {case.num_seqs}, all {case.num_heads} heads, context truncated "
+            f"to its first {tokens} of {full} tokens, per step")
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) q/k/v, shuffled block pool)",
+        "config": {"workload": case.name, "sample": desc},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "kind": "oracle",
+                         "cores": oracle.num_threads(), "sample": desc},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+# ----------------------------------------------------------------------------- main
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="long_decode", choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--no-secondary", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    rank = int(os.environ.get("RANK", 0))
+    dist_on = world > 1
+    if args.impl == "reference":
+        line = reference_arm(args, rank, world)
+    else:
+        if dist_on:
+            torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+            torch.distributed.init_process_group("nccl")
+        line = gpu_arm(args, rank, world, dist_on)
+        if dist_on:
+            torch.distributed.destroy_process_group()
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

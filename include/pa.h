@@ -1,0 +1,188 @@
+/*
+ * pa.h -- C ABI of the GB300 (sm_103a) paged-attention library.
+ *
+ * Paged attention over a block-tabled KV cache, as described on the
+ * TensorSharp "Mistral 3" model page, section 11 "Batched / paged forward
+ * (continuous batching)", and on the mistral.rs part of the "pure Rust
+ * engines" page (paged attention, KV-cache manager, prefix cache and
+ * scheduler sections).  Four operations:
+ *
+ *   pa_reshape_and_cache  write fresh K/V into cache slots through a slot map
+ *   pa_decode             one query token per sequence, split-K over the
+ *                         context, log-sum-exp reduce
+ *   pa_prefill_chunk      a chunk of query tokens per sequence: causal inside
+ *                         the chunk, full over the cached prefix
+ *   pa_copy_blocks        whole-block copies for prefix-cache reuse
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - Every tensor argument is a pointer to DEVICE memory owned by the caller,
+ *    dense row-major, 16-byte aligned.  The library allocates nothing, keeps
+ *    no state between calls and never synchronises the device.
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream) and runs asynchronously.
+ *  - The return value is PA_OK (0) or a negative PA_ERR_* code.  Argument
+ *    errors are detected on the host before anything is launched.  A failed
+ *    launch returns PA_ERR_CUDA.
+ *  - Values that only the device can see (slot numbers, block ids, context
+ *    lengths) are range-checked inside the kernels: an out-of-range value is
+ *    never dereferenced; the offending token / block is skipped and, if
+ *    `status` is not NULL, the matching PA_DEVERR_* bit is OR-ed into the
+ *    device int32 `*status`.  The caller clears *status and reads it after
+ *    synchronising.
+ *
+ * Layouts (S sequences, Hq query heads, Hkv kv heads, D head dim, bs block
+ * size, NB blocks in the pool; G = Hq / Hkv; query head h reads kv head h / G)
+ *  - key_cache, value_cache: [NB][bs][Hkv][D], the flat
+ *    [numBlocks * blockSize * numKvHeads * headDim] per-layer buffer of the
+ *    TensorSharp page, section 11.  Token slot `slot` is row slot of the
+ *    [NB * bs][Hkv][D] view: block slot / bs, offset slot % bs.
+ *  - block_tables: int32 [S][max_blocks_per_seq]; logical token j of sequence
+ *    s lives in physical block block_tables[s][j / bs] at offset j % bs.
+ *    Entries past ceil(context_lens[s] / bs) are never read.
+ *  - context_lens: int32 [S]; the number of keys the sequence's last query row
+ *    sees, the freshly written token(s) included.
+ *
+ * Supported shapes: dtype F32, F16 or BF16 (query and cache share it); D in
+ * {64, 128}; bs in {8, 16, 32} (the mistral.rs page's allowed block sizes);
+ * Hq a multiple of Hkv with G in {1, 2, 4, 8}.
+ */
+#ifndef PA_H_
+#define PA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t; declared here so the header needs no CUDA headers. */
+typedef struct CUstream_st *pa_stream_t;
+
+typedef enum { PA_F32 = 0, PA_F16 = 1, PA_BF16 = 2 } pa_dtype;
+
+enum {
+    PA_OK = 0,
+    PA_ERR_INVALID_ARG = -1, /* null / misaligned pointer, negative size, bad dtype */
+    PA_ERR_UNSUPPORTED = -2, /* head_dim, block_size or head grouping not built */
+    PA_ERR_WORKSPACE = -3,   /* workspace missing or smaller than required */
+    PA_ERR_CUDA = -4         /* a kernel launch failed (cudaGetLastError) */
+};
+
+/* Bits OR-ed into the optional device-side `*status` word. */
+enum {
+    PA_DEVERR_SLOT = 1,      /* slot_mapping entry >= num_blocks * block_size */
+    PA_DEVERR_BLOCK_ID = 2,  /* block table / block mapping id outside [0, num_blocks) */
+    PA_DEVERR_CONTEXT = 4,   /* context length < 0, > max_context_len, or beyond the block table */
+    PA_DEVERR_QUERY = 8      /* query_start_loc not monotone, or a chunk longer than its context */
+};
+
+/*
+ * pa_reshape_and_cache -- write fresh keys and values into their cache slots.
+ * TensorSharp "Mistral 3" page, section 11 (K/V scatter via slotMapping to
+ * blockId * blockSize + offset; no per-sequence extract / inject).
+ *
+ *   key, value     [num_tokens][num_kv_heads][head_dim], kv_dtype (read)
+ *   key_cache,
+ *   value_cache    [num_blocks][block_size][num_kv_heads][head_dim] (written)
+ *   slot_mapping   int64 [num_tokens]; slot < 0 skips the token (padding)
+ *
+ * Each written row is a bit copy.  Tokens must map to distinct slots (two
+ * tokens writing one slot race).  num_tokens == 0 is a no-op.
+ */
+int pa_reshape_and_cache(const void *key, const void *value, void *key_cache, void *value_cache,
+                         const int64_t *slot_mapping, int num_tokens, int num_kv_heads,
+                         int head_dim, int block_size, int num_blocks, pa_dtype kv_dtype,
+                         int32_t *status, pa_stream_t stream);
+
+/*
+ * pa_decode_workspace_size -- bytes of device workspace pa_decode needs for
+ * these sizes on the current device (0 when no split of the context is
+ * needed).  The value depends only on its arguments and the device.
+ */
+size_t pa_decode_workspace_size(int num_seqs, int num_heads, int head_dim, int max_context_len);
+
+/*
+ * pa_decode -- decode attention: one query token per sequence against every
+ * cached key of that sequence, gathered through its block table.
+ * TensorSharp "Mistral 3" page, section 11 (per-sequence paged attention over
+ * the paged K/V buffer) and sections 3 / 4.1 (standard causal GQA attention,
+ * Q scaled by 1/sqrt(headDim)).
+ *
+ *   out            [num_seqs][num_heads][head_dim], out_dtype (written)
+ *   query          [num_seqs][num_heads][head_dim], kv_dtype
+ *   key_cache,
+ *   value_cache    [num_blocks][block_size][num_kv_heads][head_dim], kv_dtype
+ *   block_tables   int32 [num_seqs][max_blocks_per_seq]
+ *   context_lens   int32 [num_seqs]; max_context_len >= every entry (host bound
+ *                  used to size the split of the context)
+ *   scale          softmax scale applied to q.k (normally 1/sqrt(head_dim))
+ *   workspace      device scratch of >= pa_decode_workspace_size(...) bytes,
+ *                  16-byte aligned (may be NULL when that size is 0); its
+ *                  contents are clobbered
+ *
+ *   out[s][h] = sum_j softmax_j(scale * q[s][h] . k_j) v_j over j < context_lens[s];
+ *   a sequence with context length 0 gets an all-zero row.
+ * Accumulation is fp32; the result does not depend on the split.
+ */
+int pa_decode(void *out, pa_dtype out_dtype, const void *query, const void *key_cache,
+              const void *value_cache, const int32_t *block_tables, int max_blocks_per_seq,
+              const int32_t *context_lens, int max_context_len, int num_seqs, int num_heads,
+              int num_kv_heads, int head_dim, int block_size, int num_blocks, float scale,
+              pa_dtype kv_dtype, void *workspace, size_t workspace_bytes, int32_t *status,
+              pa_stream_t stream);
+
+/*
+ * pa_prefill_chunk -- chunked-prefill attention.  Sequence s owns the packed
+ * query rows query_start_loc[s] .. query_start_loc[s+1]-1 (Lq_s rows, the
+ * newest tokens of the sequence, whose K/V are already in the cache).  Row i
+ * sits at absolute position context_lens[s] - Lq_s + i and attends keys
+ * 0 .. that position: full attention over the cached prefix, causal inside
+ * the chunk.  mistral.rs page, scheduling section (prompts chunked under a
+ * token budget of 4096, 512 per chunk); TensorSharp page, section 11.
+ *
+ *   out              [num_tokens][num_heads][head_dim], out_dtype (written)
+ *   query            [num_tokens][num_heads][head_dim], kv_dtype (F16 or BF16)
+ *   query_start_loc  int32 [num_seqs + 1], non-decreasing, [0] = 0,
+ *                    [num_seqs] = num_tokens
+ *   max_query_len    >= every Lq_s (host bound used to size the grid)
+ *   other arguments  as for pa_decode
+ *
+ * Tensor-core MMA with fp32 accumulation; the softmax weights are rounded to
+ * the input dtype before the P.V product.
+ */
+int pa_prefill_chunk(void *out, pa_dtype out_dtype, const void *query,
+                     const int32_t *query_start_loc, int num_tokens, int max_query_len,
+                     const void *key_cache, const void *value_cache, const int32_t *block_tables,
+                     int max_blocks_per_seq, const int32_t *context_lens, int max_context_len,
+                     int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size,
+                     int num_blocks, float scale, pa_dtype kv_dtype, int32_t *status,
+                     pa_stream_t stream);
+
+/*
+ * pa_copy_blocks -- copy whole cache blocks, K and V, for prefix-cache reuse
+ * (mistral.rs page, block-hash prefix cache: full blocks are shared by
+ * content; a copy gives a sequence its own writable copy of a shared block).
+ *
+ *   block_mapping  int64 [num_pairs][2] = (src, dst) block ids
+ *
+ * Destinations must be distinct and must not appear as sources (then the
+ * result equals copying the pairs one after another); otherwise the result
+ * is undefined.  num_pairs == 0 is a no-op.
+ */
+int pa_copy_blocks(void *key_cache, void *value_cache, const int64_t *block_mapping, int num_pairs,
+                   int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                   pa_dtype kv_dtype, int32_t *status, pa_stream_t stream);
+
+/* Static description of a PA_* return code. */
+const char *pa_status_string(int code);
+
+/* Library version as major * 10000 + minor * 100 + patch. */
+int pa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H_ */

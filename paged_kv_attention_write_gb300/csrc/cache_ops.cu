@@ -1,0 +1,98 @@
+// cache_ops.cu -- the two data-movement operations on the paged KV pool.
+//
+// reshape_and_cache: fresh K/V rows scattered to slot = blockId * blockSize +
+//   offset (TensorSharp "Mistral 3" page, section 11, K/V scatter via
+//   slotMapping).  In the [NB][bs][Hkv][D] pool a token's Hkv*D elements are
+//   one contiguous row, so each token is one contiguous 16-byte-vector copy.
+// copy_blocks: whole-block K and V copies for prefix-cache reuse (mistral.rs
+//   page, block-hash prefix cache).  A block is bs*Hkv*D contiguous elements.
+//
+// Both are HBM-bound bit copies: 16-byte vector loads and stores, coalesced
+// along the row; no arithmetic on the elements.
+#include "common.cuh"
+
+namespace pa {
+namespace {
+
+constexpr int kCopyThreads = 128;
+
+// One CTA per fresh token; the row is row_bytes (a multiple of 16).
+__global__ void __launch_bounds__(kCopyThreads)
+reshape_and_cache_kernel(const uint4 *__restrict__ key, const uint4 *__restrict__ value,
+                         uint4 *__restrict__ key_cache, uint4 *__restrict__ value_cache,
+                         const int64_t *__restrict__ slot_mapping, int vecs_per_row,
+                         int64_t num_slots, int32_t *status) {
+    const int t = blockIdx.x;
+    const int64_t slot = slot_mapping[t];
+    if (slot < 0) return;  // padding token
+    if (slot >= num_slots) {
+        if (threadIdx.x == 0) report(status, PA_DEVERR_SLOT);
+        return;
+    }
+    const uint4 *ks = key + (int64_t)t * vecs_per_row;
+    const uint4 *vs = value + (int64_t)t * vecs_per_row;
+    uint4 *kd = key_cache + slot * vecs_per_row;
+    uint4 *vd = value_cache + slot * vecs_per_row;
+    for (int i = threadIdx.x; i < vecs_per_row; i += kCopyThreads) {
+        uint4 k = ks[i];
+        uint4 v = vs[i];
+        kd[i] = k;
+        vd[i] = v;
+    }
+}
+
+// grid = (num_pairs, chunks); each CTA copies one chunk of one block, K and V.
+__global__ void __launch_bounds__(kCopyThreads)
+copy_blocks_kernel(uint4 *__restrict__ key_cache, uint4 *__restrict__ value_cache,
+                   const int64_t *__restrict__ block_mapping, int64_t vecs_per_block,
+                   int64_t vecs_per_chunk, int num_blocks, int32_t *status) {
+    const int p = blockIdx.x;
+    const int64_t src = block_mapping[2 * p];
+    const int64_t dst = block_mapping[2 * p + 1];
+    if (src < 0 || dst < 0 || src >= num_blocks || dst >= num_blocks) {
+        if (threadIdx.x == 0 && blockIdx.y == 0) report(status, PA_DEVERR_BLOCK_ID);
+        return;
+    }
+    const int64_t begin = (int64_t)blockIdx.y * vecs_per_chunk;
+    const int64_t end = min(vecs_per_block, begin + vecs_per_chunk);
+    const uint4 *ks = key_cache + src * vecs_per_block;
+    const uint4 *vs = value_cache + src * vecs_per_block;
+    uint4 *kd = key_cache + dst * vecs_per_block;
+    uint4 *vd = value_cache + dst * vecs_per_block;
+    for (int64_t i = begin + threadIdx.x; i < end; i += kCopyThreads) {
+        uint4 k = ks[i];
+        uint4 v = vs[i];
+        kd[i] = k;
+        vd[i] = v;
+    }
+}
+
+}  // namespace
+
+int launch_reshape_and_cache(const void *key, const void *value, void *key_cache,
+                             void *value_cache, const int64_t *slot_mapping, int num_tokens,
+                             int row_bytes, int block_size, int num_blocks, int32_t *status,
+                             cudaStream_t stream) {
+    if (num_tokens == 0) return PA_OK;
+    reshape_and_cache_kernel<<<num_tokens, kCopyThreads, 0, stream>>>(
+        static_cast<const uint4 *>(key), static_cast<const uint4 *>(value),
+        static_cast<uint4 *>(key_cache), static_cast<uint4 *>(value_cache), slot_mapping,
+        row_bytes / 16, (int64_t)num_blocks * block_size, status);
+    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+int launch_copy_blocks(void *key_cache, void *value_cache, const int64_t *block_mapping,
+                       int num_pairs, int64_t block_bytes, int num_blocks, int32_t *status,
+                       cudaStream_t stream) {
+    if (num_pairs == 0) return PA_OK;
+    const int64_t vecs = block_bytes / 16;
+    const int64_t per_chunk = kCopyThreads * 8;  // 16 KB of K and 16 KB of V per CTA
+    const int64_t chunks = (vecs + per_chunk - 1) / per_chunk;
+    dim3 grid(num_pairs, (unsigned)chunks);
+    copy_blocks_kernel<<<grid, kCopyThreads, 0, stream>>>(
+        static_cast<uint4 *>(key_cache), static_cast<uint4 *>(value_cache), block_mapping, vecs,
+        per_chunk, num_blocks, status);
+    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+}  // namespace pa

@@ -1,0 +1,150 @@
+// common.cuh -- device helpers shared by the paged-attention kernels.
+//
+// Element formats, 16-byte vector loads, the device-side status word and the
+// internal launcher declarations.  Nothing here is part of the public ABI
+// (include/pa.h is).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/pa.h"
+
+namespace pa {
+
+constexpr unsigned kFullMask = 0xffffffffu;
+constexpr float kLog2e = 1.4426950408889634f;
+
+// ---------------------------------------------------------------- element formats
+// Tag types: a 16-byte vector holds kPerVec elements of the format.
+struct F32 {
+    using storage = float;
+    static constexpr int kBytes = 4;
+    static constexpr int kPerVec = 4;
+};
+struct F16 {
+    using storage = __half;
+    static constexpr int kBytes = 2;
+    static constexpr int kPerVec = 8;
+};
+struct BF16 {
+    using storage = __nv_bfloat16;
+    static constexpr int kBytes = 2;
+    static constexpr int kPerVec = 8;
+};
+
+// Widen one 16-byte vector to floats.
+__device__ __forceinline__ void widen(F32, const uint4 &v, float *f) {
+    f[0] = __uint_as_float(v.x);
+    f[1] = __uint_as_float(v.y);
+    f[2] = __uint_as_float(v.z);
+    f[3] = __uint_as_float(v.w);
+}
+__device__ __forceinline__ void widen_pair_bf16(uint32_t u, float &lo, float &hi) {
+    // bf16 is the top half of an fp32 word: widening is a shift / mask.
+    lo = __uint_as_float(u << 16);
+    hi = __uint_as_float(u & 0xffff0000u);
+}
+__device__ __forceinline__ void widen(BF16, const uint4 &v, float *f) {
+    widen_pair_bf16(v.x, f[0], f[1]);
+    widen_pair_bf16(v.y, f[2], f[3]);
+    widen_pair_bf16(v.z, f[4], f[5]);
+    widen_pair_bf16(v.w, f[6], f[7]);
+}
+__device__ __forceinline__ void widen_pair_f16(uint32_t u, float &lo, float &hi) {
+    __half2 h = *reinterpret_cast<__half2 *>(&u);
+    float2 f = __half22float2(h);
+    lo = f.x;
+    hi = f.y;
+}
+__device__ __forceinline__ void widen(F16, const uint4 &v, float *f) {
+    widen_pair_f16(v.x, f[0], f[1]);
+    widen_pair_f16(v.y, f[2], f[3]);
+    widen_pair_f16(v.z, f[4], f[5]);
+    widen_pair_f16(v.w, f[6], f[7]);
+}
+
+// Store n (even) floats, rounded to the output format.
+__device__ __forceinline__ void store_out(float *p, float a, float b) {
+    *reinterpret_cast<float2 *>(p) = make_float2(a, b);
+}
+__device__ __forceinline__ void store_out(__half *p, float a, float b) {
+    *reinterpret_cast<__half2 *>(p) = __floats2half2_rn(a, b);
+}
+__device__ __forceinline__ void store_out(__nv_bfloat16 *p, float a, float b) {
+    *reinterpret_cast<__nv_bfloat162 *>(p) = __floats2bfloat162_rn(a, b);
+}
+
+// ---------------------------------------------------------------- memory helpers
+// Streaming 16-byte load through the non-coherent path, not kept in L1.
+__device__ __forceinline__ uint4 ldg_stream(const void *p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void report(int32_t *status, int bit) {
+    if (status) atomicOr(status, bit);
+}
+
+}  // namespace pa
+
+// ---------------------------------------------------------------- internal launchers
+// Called by the C-ABI layer after host-side validation.  Each returns a
+// PA_* code (PA_ERR_CUDA when the launch itself failed).
+namespace pa {
+
+struct DecodeArgs {
+    void *out;
+    pa_dtype out_dtype;
+    const void *query;
+    const void *key_cache;
+    const void *value_cache;
+    const int32_t *block_tables;
+    int max_blocks_per_seq;
+    const int32_t *context_lens;
+    int max_context_len;
+    int num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_blocks;
+    float scale;
+    pa_dtype kv_dtype;
+    void *workspace;
+    size_t workspace_bytes;
+    int32_t *status;
+    cudaStream_t stream;
+};
+
+struct PrefillArgs {
+    void *out;
+    pa_dtype out_dtype;
+    const void *query;
+    const int32_t *query_start_loc;
+    int num_tokens, max_query_len;
+    const void *key_cache;
+    const void *value_cache;
+    const int32_t *block_tables;
+    int max_blocks_per_seq;
+    const int32_t *context_lens;
+    int max_context_len;
+    int num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_blocks;
+    float scale;
+    pa_dtype kv_dtype;
+    int32_t *status;
+    cudaStream_t stream;
+};
+
+int launch_reshape_and_cache(const void *key, const void *value, void *key_cache,
+                             void *value_cache, const int64_t *slot_mapping, int num_tokens,
+                             int row_bytes, int block_size, int num_blocks, int32_t *status,
+                             cudaStream_t stream);
+int launch_copy_blocks(void *key_cache, void *value_cache, const int64_t *block_mapping,
+                       int num_pairs, int64_t block_bytes, int num_blocks, int32_t *status,
+                       cudaStream_t stream);
+size_t decode_workspace_bytes(int num_seqs, int num_heads, int head_dim, int max_context_len);
+int launch_decode(const DecodeArgs &a);
+int launch_prefill(const PrefillArgs &a);
+
+}  // namespace pa

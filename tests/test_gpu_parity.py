@@ -1,0 +1,201 @@
+"""GPU parity: the CUDA library (called through its C ABI) against the fp64 oracle on
+the same seeded inputs.  Cache writes and block copies bit-exact; attention within
+max-abs 5e-3 / mean-abs 5e-4 in fp32 (tighter for fp32 inputs)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from paged_steps import (assert_attention_close, bits, check_case, gpu_step, oracle_step)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _need_gpu(cuda_ok):
+    yield
+
+
+# ----------------------------------------------------------------------------- the five workloads
+
+def test_tiny_decode(oracle_mod):
+    case = workloads.tiny_decode()
+    mx, _ = check_case(case, oracle_mod)
+    assert mx < 1e-5  # fp32 inputs, fp32 accumulation
+
+
+def test_decode_batch_full_size(oracle_mod):
+    check_case(workloads.decode_batch(), oracle_mod)
+
+
+def test_long_decode_full_size(oracle_mod):
+    check_case(workloads.long_decode(), oracle_mod)
+
+
+def test_prefill_chunk_full_size(oracle_mod):
+    check_case(workloads.prefill_chunk(), oracle_mod)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16], ids=["bf16", "fp16"])
+@pytest.mark.parametrize("bs", [8, 16, 32])
+def test_stress_full_size(oracle_mod, bs, dtype):
+    case = workloads.stress_decode(block_size=bs, dtype=dtype)
+    assert case.block_mapping is not None and case.block_mapping.shape[0] > 0
+    check_case(case, oracle_mod)
+
+
+# ----------------------------------------------------------------------------- decode shapes and edges
+
+DECODE_LENS = [0, 1, 7, 8, 31, 32, 33, 511, 512, 513, 1100, 2049]
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.float16, torch.bfloat16],
+                         ids=["fp32", "fp16", "bf16"])
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("G", [1, 2, 4, 8])
+@pytest.mark.parametrize("bs", [8, 16, 32])
+def test_decode_shape_sweep(oracle_mod, dtype, D, G, bs):
+    """Every built (dtype, head dim, group, block size) on ragged context lengths that
+    cover single-token, exact-block, block+1 and multi-partition cases."""
+    Hkv = 2
+    case = workloads.make_decode_case("sweep", DECODE_LENS, bs, Hkv * G, Hkv, D, dtype,
+                                      seed=D * 100 + G * 10 + bs, free_frac=0.1)
+    mx, mn = check_case(case, oracle_mod)
+    if dtype == torch.float32:
+        assert mx < 1e-5
+
+
+def test_decode_zero_context_gives_zero_row(oracle_mod):
+    case = workloads.make_decode_case("zero", [40, 3, 700], 16, 8, 2, 128, torch.bfloat16, 9)
+    case.context_lens[1] = 0       # sequence 1 attends nothing
+    case.slot_mapping[1] = -1      # and writes nothing
+    out, kc, vc, status = gpu_step(case)
+    ref, okc, ovc = oracle_step(case, oracle_mod)
+    assert status == 0
+    assert torch.all(out[1] == 0)
+    assert torch.equal(bits(kc), bits(okc))
+    assert_attention_close(out, ref)
+
+
+def test_decode_is_deterministic_and_placement_independent(oracle_mod):
+    """Two runs are byte-identical; the same logical K/V under another block placement
+    gives byte-identical output (the arithmetic order depends on logical positions only)."""
+    a = workloads.make_decode_case("p", [900, 77, 1500, 2], 16, 16, 4, 128, torch.bfloat16, 21)
+    o1, *_ = gpu_step(a)
+    o2, *_ = gpu_step(a)
+    assert torch.equal(bits(o1), bits(o2))
+    # re-place every block of a at new physical ids
+    NB = a.num_blocks
+    perm = torch.from_numpy(np.random.default_rng(5).permutation(NB)).to(torch.int64)
+    b = workloads.make_decode_case("p", [900, 77, 1500, 2], 16, 16, 4, 128, torch.bfloat16, 21)
+    b.key_cache = torch.empty_like(a.key_cache)
+    b.value_cache = torch.empty_like(a.value_cache)
+    b.key_cache[perm] = a.key_cache
+    b.value_cache[perm] = a.value_cache
+    valid = a.block_tables >= 0
+    b.block_tables = torch.where(valid, perm[a.block_tables.clamp(min=0).long()].to(torch.int32),
+                                 a.block_tables)
+    bs = a.block_size
+    b.slot_mapping = perm[a.slot_mapping // bs] * bs + a.slot_mapping % bs
+    o3, *_ = gpu_step(b)
+    assert torch.equal(bits(o1), bits(o3))
+
+
+@pytest.mark.parametrize("out_dtype", [torch.float16, torch.bfloat16])
+def test_decode_low_precision_output_is_rounded_fp32(oracle_mod, out_dtype):
+    case = workloads.make_decode_case("o", [100, 1000, 3000], 32, 32, 8, 128, torch.bfloat16, 4)
+    o32, *_ = gpu_step(case, torch.float32)
+    olo, *_ = gpu_step(case, out_dtype)
+    assert torch.equal(bits(olo), bits(o32.to(out_dtype)))
+
+
+def test_decode_aliased_block_tables(oracle_mod):
+    """Read-only sharing: several block tables point at the same physical prefix blocks."""
+    case = workloads.make_decode_case("alias", list(range(100, 2100, 100)), 16, 32, 8, 128,
+                                      torch.bfloat16, 13, free_frac=0.2, alias_frac=0.3)
+    assert case.meta["aliased"]
+    check_case(case, oracle_mod)
+
+
+# ----------------------------------------------------------------------------- prefill shapes and edges
+
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16], ids=["fp16", "bf16"])
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("G", [1, 2, 4, 8])
+def test_prefill_shape_sweep(oracle_mod, dtype, D, G):
+    """Ragged chunks (1 row, sub-tile, multi-tile with tail) over prefixes that are empty,
+    sub-block, and multi-tile."""
+    Hkv = 2
+    prefix = [0, 5, 64, 300, 0, 1000]
+    chunk = [1, 17, 64, 130, 200, 3]
+    for bs in (8, 16, 32):
+        case = workloads.make_prefill_case("pf", prefix, chunk, bs, Hkv * G, Hkv, D, dtype,
+                                           seed=bs + D + G, free_frac=0.1)
+        check_case(case, oracle_mod)
+
+
+def test_prefill_single_row_matches_decode(oracle_mod):
+    """A chunk of one row is a decode step: both kernels agree within tolerance."""
+    d = workloads.make_decode_case("pd", [63, 500, 1200], 16, 32, 8, 128, torch.bfloat16, 17)
+    od, *_ = gpu_step(d)
+    p = workloads.make_decode_case("pd", [63, 500, 1200], 16, 32, 8, 128, torch.bfloat16, 17)
+    import paged_kv_attention_write_gb300 as pa
+    dev = "cuda"
+    kc, vc = p.key_cache.to(dev), p.value_cache.to(dev)
+    pa.pa_reshape_and_cache(p.new_key.to(dev), p.new_value.to(dev), kc, vc, p.slot_mapping.to(dev))
+    out = torch.empty(p.query.shape, dtype=torch.float32, device=dev)
+    pa.pa_prefill_chunk(out, p.query.to(dev), p.query_start_loc.to(dev), 1, kc, vc,
+                        p.block_tables.to(dev), p.context_lens.to(dev), p.max_context_len, p.scale)
+    torch.cuda.synchronize()
+    assert (out.cpu() - od).abs().max().item() < 5e-3
+
+
+# ----------------------------------------------------------------------------- device-side range checks
+
+def test_device_checks_report_instead_of_reading_out_of_range():
+    """Bad block ids, slots, copy pairs and context lengths set status bits; nothing
+    outside the buffers is read or written (the pools keep their bytes)."""
+    import paged_kv_attention_write_gb300 as pa
+    case = workloads.make_decode_case("bad", [40, 90], 16, 8, 2, 128, torch.bfloat16, 3)
+    dev = "cuda"
+    kc, vc = case.key_cache.to(dev), case.value_cache.to(dev)
+    before = bits(kc).clone()
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    NB = case.num_blocks
+    # slot past the pool
+    pa.pa_reshape_and_cache(case.new_key[:1].to(dev), case.new_value[:1].to(dev), kc, vc,
+                            torch.tensor([NB * 16 + 3], dtype=torch.int64, device=dev), status=st)
+    torch.cuda.synchronize()
+    assert st.item() & 1 and torch.equal(bits(kc), before)
+    # copy pair with a block id past the pool
+    st.zero_()
+    pa.pa_copy_blocks(kc, vc, torch.tensor([[0, NB + 2]], dtype=torch.int64, device=dev), status=st)
+    torch.cuda.synchronize()
+    assert st.item() & 2 and torch.equal(bits(kc), before)
+    # block table entry past the pool, and a context longer than the table
+    bt = case.block_tables.clone()
+    bt[0, 1] = NB + 100
+    cl = case.context_lens.clone()
+    cl[1] = bt.shape[1] * 16 + 50
+    out = torch.empty(case.query.shape, dtype=torch.float32, device=dev)
+    ws = torch.empty(1 << 20, dtype=torch.uint8, device=dev)
+    st.zero_()
+    pa.pa_decode(out, case.query.to(dev), kc, vc, bt.to(dev), cl.to(dev), int(cl.max()),
+                 case.scale, workspace=ws, status=st)
+    torch.cuda.synchronize()
+    assert st.item() & 2 and st.item() & 4
+    st.zero_()
+    qsl = torch.tensor([0, 1, 5], dtype=torch.int32, device=dev)  # runs past the 2 query rows
+    pa.pa_prefill_chunk(out, case.query.to(dev), qsl, 4, kc, vc, bt.to(dev), cl.to(dev),
+                        int(cl.max()), case.scale, status=st)
+    torch.cuda.synchronize()
+    assert st.item() & 8
+
+
+def test_reshape_and_cache_skips_negative_slots(oracle_mod):
+    case = workloads.make_decode_case("neg", [10, 20, 30, 40], 8, 4, 2, 64, torch.float16, 8)
+    case.slot_mapping[2] = -1
+    case.context_lens[2] = int(case.cached_lens[2])  # nothing fresh for sequence 2
+    check_case(case, oracle_mod)
