@@ -177,7 +177,8 @@ class DecodeStep:
         self.nv = case.new_value.to(device)
         self.slots = case.slot_mapping.to(device)
         self.out = torch.empty(tuple(case.query.shape), dtype=torch.float32, device=device)
-        nbytes = pa.pa_decode_workspace_size(case.num_seqs, case.num_heads, case.head_dim,
+        nbytes = pa.pa_decode_workspace_size(case.num_seqs, case.num_heads, case.num_kv_heads,
+                                             case.head_dim,
                                              case.max_context_len)
         self.ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=device)
         self.max_ctx = case.max_context_len
@@ -210,8 +211,8 @@ class DecodeStep:
         return self.h_out.numel() * self.h_out.element_size()
 
     def launches_per_step(self):
-        np_ = math.ceil(self.max_ctx / 512)
-        return 2 + (1 if np_ > 1 else 0)
+        # pa_reshape_and_cache: 1 kernel; pa_decode: plan, split, reduce
+        return 4
 
 
 def _barrier(dist_on):

@@ -45,7 +45,8 @@
  *
  * Supported shapes: dtype F32, F16 or BF16 (query and cache share it); D in
  * {64, 128}; bs in {8, 16, 32} (the mistral.rs page's allowed block sizes);
- * Hq a multiple of Hkv with G in {1, 2, 4, 8}.
+ * Hq a multiple of Hkv with G = Hq / Hkv in {1, 2, 4, 8}; Hkv in {1, 2, 4} or
+ * a multiple of 8; num_blocks * block_size < 2^31.
  */
 #ifndef PA_H_
 #define PA_H_
@@ -75,7 +76,9 @@ enum {
     PA_DEVERR_SLOT = 1,      /* slot_mapping entry >= num_blocks * block_size */
     PA_DEVERR_BLOCK_ID = 2,  /* block table / block mapping id outside [0, num_blocks) */
     PA_DEVERR_CONTEXT = 4,   /* context length < 0, > max_context_len, or beyond the block table */
-    PA_DEVERR_QUERY = 8      /* query_start_loc not monotone, or a chunk longer than its context */
+    PA_DEVERR_QUERY = 8,     /* query_start_loc not monotone, or a chunk longer than its context */
+    PA_DEVERR_TIMEOUT = 16   /* a bounded wait inside a kernel gave up (internal error; the
+                                kernel returned instead of hanging) */
 };
 
 /*
@@ -98,10 +101,14 @@ int pa_reshape_and_cache(const void *key, const void *value, void *key_cache, vo
 
 /*
  * pa_decode_workspace_size -- bytes of device workspace pa_decode needs for
- * these sizes on the current device (0 when no split of the context is
- * needed).  The value depends only on its arguments and the device.
+ * these sizes on the current device (0 only when num_seqs == 0).  The value
+ * depends on its arguments and on the device's SM count (the split of the
+ * contexts is balanced over one CTA per SM); on a machine without a visible
+ * device it returns an upper bound.  Returns 0 for arguments pa_decode would
+ * reject.
  */
-size_t pa_decode_workspace_size(int num_seqs, int num_heads, int head_dim, int max_context_len);
+size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                                int max_context_len);
 
 /*
  * pa_decode -- decode attention: one query token per sequence against every
@@ -119,8 +126,8 @@ size_t pa_decode_workspace_size(int num_seqs, int num_heads, int head_dim, int m
  *                  used to size the split of the context)
  *   scale          softmax scale applied to q.k (normally 1/sqrt(head_dim))
  *   workspace      device scratch of >= pa_decode_workspace_size(...) bytes,
- *                  16-byte aligned (may be NULL when that size is 0); its
- *                  contents are clobbered
+ *                  16-byte aligned, owned by the caller; its contents are
+ *                  clobbered, and two calls in flight must not share it
  *
  *   out[s][h] = sum_j softmax_j(scale * q[s][h] . k_j) v_j over j < context_lens[s];
  *   a sequence with context length 0 gets an all-zero row.

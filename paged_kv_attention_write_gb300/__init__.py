@@ -1,7 +1,7 @@
 """GB300 (sm_103a) paged attention over a block-tabled KV cache.
 
 A thin ctypes binding over the C ABI in ``include/pa.h`` (``libpa.so``, built
-in-tree by ``paged_kv_attention_write_gb300.build``).  The Python functions
+in-tree by ``paged_kv_attention_write_gb300/build.py``).  The Python functions
 carry the C names and do argument marshalling only: shapes come from the
 tensors, pointers from ``data_ptr()``, the stream from torch's current CUDA
 stream.  Every step of the computation runs in the CUDA kernels; there is no
@@ -35,13 +35,13 @@ _LIB_PATH = Path(__file__).resolve().parent / "libpa.so"
 if not _LIB_PATH.exists():
     raise ImportError(
         f"{_LIB_PATH} is missing: build the CUDA library first "
-        "(python -m paged_kv_attention_write_gb300.build); there is no fallback")
+        "(python paged_kv_attention_write_gb300/build.py); there is no fallback")
 _lib = ctypes.CDLL(str(_LIB_PATH))
 
 _vp, _i32, _f32, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
 _lib.pa_reshape_and_cache.argtypes = [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32,
                                       _vp, _vp]
-_lib.pa_decode_workspace_size.argtypes = [_i32, _i32, _i32, _i32]
+_lib.pa_decode_workspace_size.argtypes = [_i32, _i32, _i32, _i32, _i32]
 _lib.pa_decode_workspace_size.restype = _sz
 _lib.pa_decode.argtypes = [_vp, _i32, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32,
                            _i32, _i32, _f32, _i32, _vp, _sz, _vp, _vp]
@@ -108,9 +108,10 @@ def pa_reshape_and_cache(key, value, key_cache, value_cache, slot_mapping, *, st
                                      _ptr(status), _stream(stream)), "pa_reshape_and_cache")
 
 
-def pa_decode_workspace_size(num_seqs: int, num_heads: int, head_dim: int,
+def pa_decode_workspace_size(num_seqs: int, num_heads: int, num_kv_heads: int, head_dim: int,
                              max_context_len: int) -> int:
-    return int(_lib.pa_decode_workspace_size(num_seqs, num_heads, head_dim, max_context_len))
+    return int(_lib.pa_decode_workspace_size(num_seqs, num_heads, num_kv_heads, head_dim,
+                                             max_context_len))
 
 
 def pa_decode(out, query, key_cache, value_cache, block_tables, context_lens, max_context_len: int,

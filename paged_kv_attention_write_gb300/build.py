@@ -2,7 +2,8 @@
 
 Each ``csrc/*.cu`` translation unit is compiled in parallel, then linked into
 one shared library next to this file.  Object files go to ``_build/`` at the
-repository root.  ``python -m paged_kv_attention_write_gb300.build`` runs it.
+repository root.  ``python paged_kv_attention_write_gb300/build.py [-v]`` runs it (the
+package itself cannot be imported before the library exists).
 """
 from __future__ import annotations
 

@@ -22,6 +22,8 @@ reshape_and_cache_kernel(const uint4 *__restrict__ key, const uint4 *__restrict_
                          uint4 *__restrict__ key_cache, uint4 *__restrict__ value_cache,
                          const int64_t *__restrict__ slot_mapping, int vecs_per_row,
                          int64_t num_slots, int32_t *status) {
+    pdl_wait_previous();
+    pdl_launch_dependents();
     const int t = blockIdx.x;
     const int64_t slot = slot_mapping[t];
     if (slot < 0) return;  // padding token
@@ -46,6 +48,8 @@ __global__ void __launch_bounds__(kCopyThreads)
 copy_blocks_kernel(uint4 *__restrict__ key_cache, uint4 *__restrict__ value_cache,
                    const int64_t *__restrict__ block_mapping, int64_t vecs_per_block,
                    int64_t vecs_per_chunk, int num_blocks, int32_t *status) {
+    pdl_wait_previous();
+    pdl_launch_dependents();
     const int p = blockIdx.x;
     const int64_t src = block_mapping[2 * p];
     const int64_t dst = block_mapping[2 * p + 1];
@@ -74,11 +78,12 @@ int launch_reshape_and_cache(const void *key, const void *value, void *key_cache
                              int row_bytes, int block_size, int num_blocks, int32_t *status,
                              cudaStream_t stream) {
     if (num_tokens == 0) return PA_OK;
-    reshape_and_cache_kernel<<<num_tokens, kCopyThreads, 0, stream>>>(
+    const cudaError_t e = launch_pdl(
+        reshape_and_cache_kernel, dim3(num_tokens), dim3(kCopyThreads), 0, stream,
         static_cast<const uint4 *>(key), static_cast<const uint4 *>(value),
         static_cast<uint4 *>(key_cache), static_cast<uint4 *>(value_cache), slot_mapping,
         row_bytes / 16, (int64_t)num_blocks * block_size, status);
-    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 int launch_copy_blocks(void *key_cache, void *value_cache, const int64_t *block_mapping,
@@ -89,10 +94,11 @@ int launch_copy_blocks(void *key_cache, void *value_cache, const int64_t *block_
     const int64_t per_chunk = kCopyThreads * 8;  // 16 KB of K and 16 KB of V per CTA
     const int64_t chunks = (vecs + per_chunk - 1) / per_chunk;
     dim3 grid(num_pairs, (unsigned)chunks);
-    copy_blocks_kernel<<<grid, kCopyThreads, 0, stream>>>(
-        static_cast<uint4 *>(key_cache), static_cast<uint4 *>(value_cache), block_mapping, vecs,
-        per_chunk, num_blocks, status);
-    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+    const cudaError_t e = launch_pdl(copy_blocks_kernel, grid, dim3(kCopyThreads), 0, stream,
+                                     static_cast<uint4 *>(key_cache),
+                                     static_cast<uint4 *>(value_cache), block_mapping, vecs,
+                                     per_chunk, num_blocks, status);
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 }  // namespace pa

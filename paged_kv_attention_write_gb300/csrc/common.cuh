@@ -10,6 +10,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/pa.h"
 
 namespace pa {
@@ -91,6 +93,34 @@ __device__ __forceinline__ void report(int32_t *status, int bit) {
     if (status) atomicOr(status, bit);
 }
 
+// Programmatic dependent launch.  Every kernel of the library is launched with
+// launch_pdl (below) and calls pdl_wait_previous() before it touches memory that
+// an earlier kernel in the stream may write; pdl_launch_dependents() lets the
+// next kernel's launch and prologue overlap this one.
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait_previous() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+template <class... KArgs, class... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args &&...args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+    return e == cudaSuccess ? cudaGetLastError() : e;
+}
+
 }  // namespace pa
 
 // ---------------------------------------------------------------- internal launchers
@@ -143,7 +173,8 @@ int launch_reshape_and_cache(const void *key, const void *value, void *key_cache
 int launch_copy_blocks(void *key_cache, void *value_cache, const int64_t *block_mapping,
                        int num_pairs, int64_t block_bytes, int num_blocks, int32_t *status,
                        cudaStream_t stream);
-size_t decode_workspace_bytes(int num_seqs, int num_heads, int head_dim, int max_context_len);
+size_t decode_workspace_bytes(int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                              int max_context_len);
 int launch_decode(const DecodeArgs &a);
 int launch_prefill(const PrefillArgs &a);
 

@@ -26,7 +26,8 @@ bool block_size_ok(int b) { return b == 8 || b == 16 || b == 32; }
 bool group_ok(int hq, int hkv) {
     if (hq <= 0 || hkv <= 0 || hq % hkv) return false;
     const int g = hq / hkv;
-    return g == 1 || g == 2 || g == 4 || g == 8;
+    const bool kv_ok = hkv <= 8 ? 8 % hkv == 0 : hkv % 8 == 0;
+    return kv_ok && (g == 1 || g == 2 || g == 4 || g == 8);
 }
 
 // Shared checks of the attention calls' cache / table arguments.
@@ -43,7 +44,9 @@ int check_attention(const void *out, pa_dtype out_dtype, const void *query, cons
     if (num_heads % num_kv_heads) return PA_ERR_INVALID_ARG;
     if (!head_dim_ok(head_dim) || !block_size_ok(block_size) || !group_ok(num_heads, num_kv_heads))
         return PA_ERR_UNSUPPORTED;
-    if ((int64_t)max_blocks_per_seq * block_size > INT32_MAX) return PA_ERR_INVALID_ARG;
+    if ((int64_t)max_blocks_per_seq * block_size > INT32_MAX ||
+        (int64_t)num_blocks * block_size > INT32_MAX)
+        return PA_ERR_INVALID_ARG;
     if (num_seqs == 0) return PA_OK;
     if (!out || !query || !key_cache || !value_cache || !block_tables || !context_lens)
         return PA_ERR_INVALID_ARG;
@@ -105,9 +108,12 @@ int pa_copy_blocks(void *key_cache, void *value_cache, const int64_t *block_mapp
                                   num_blocks, status, reinterpret_cast<cudaStream_t>(stream));
 }
 
-size_t pa_decode_workspace_size(int num_seqs, int num_heads, int head_dim, int max_context_len) {
-    if (num_seqs <= 0 || num_heads <= 0 || head_dim <= 0 || max_context_len <= 0) return 0;
-    return pa::decode_workspace_bytes(num_seqs, num_heads, head_dim, max_context_len);
+size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                                int max_context_len) {
+    if (num_seqs <= 0 || num_seqs > 65535 || max_context_len < 0 || !head_dim_ok(head_dim) ||
+        !group_ok(num_heads, num_kv_heads))
+        return 0;
+    return pa::decode_workspace_bytes(num_seqs, num_heads, num_kv_heads, head_dim, max_context_len);
 }
 
 int pa_decode(void *out, pa_dtype out_dtype, const void *query, const void *key_cache,
@@ -122,9 +128,7 @@ int pa_decode(void *out, pa_dtype out_dtype, const void *query, const void *key_
                              kv_dtype);
     if (rc != PA_OK || num_seqs == 0) return rc;
     if (!aligned(status, 4)) return PA_ERR_INVALID_ARG;
-    const size_t need = pa_decode_workspace_size(num_seqs, num_heads, head_dim, max_context_len);
-    if (need > 0 && (!workspace || !aligned(workspace, 16) || workspace_bytes < need))
-        return PA_ERR_WORKSPACE;
+    if (!workspace || !aligned(workspace, 16)) return PA_ERR_WORKSPACE;
     pa::DecodeArgs a{out,          out_dtype,      query,     key_cache,    value_cache,
                      block_tables, max_blocks_per_seq, context_lens, max_context_len,
                      num_seqs,     num_heads,      num_kv_heads, head_dim,  block_size,

@@ -122,6 +122,8 @@ prefill_kernel(const PrefillParams p) {
     const uint32_t sK0 = sQ + kBM * D * 2;
     const uint32_t sV0 = sK0 + 2 * kBN * D * 2;
 
+    pdl_wait_previous();
+    pdl_launch_dependents();
     const int g = blockIdx.y, s = blockIdx.z;
     const int qt = gridDim.x - 1 - blockIdx.x;  // heaviest (latest) tiles first
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
@@ -336,8 +338,9 @@ int launch_typed(const PrefillParams &prm, int max_query_len, int num_seqs, cuda
         configured = true;
     }
     dim3 grid((max_query_len + TT - 1) / TT, prm.num_kv_heads, num_seqs);
-    prefill_kernel<T, D, G><<<grid, kPfThreads, smem, st>>>(prm);
-    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+    return launch_pdl(prefill_kernel<T, D, G>, grid, dim3(kPfThreads), smem, st, prm) == cudaSuccess
+               ? PA_OK
+               : PA_ERR_CUDA;
 }
 
 template <class T, int D>

@@ -1,0 +1,50 @@
+// tma_host.cu -- host-side helpers for the TMA kernels: tensor-map encoding
+// (through the driver entry point, so the library needs no libcuda link) and
+// the device's SM count.
+#include <cudaTypedefs.h>
+
+#include "tma.cuh"
+
+namespace pa {
+
+namespace {
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+}  // namespace
+
+int make_kv_tensor_map(CUtensorMap *map, const void *base, pa_dtype dtype, int head_dim,
+                       int num_kv_heads, int64_t rows, int box_heads, int box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return PA_ERR_CUDA;
+    CUtensorMapDataType dt = dtype == PA_F32   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                             : dtype == PA_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                               : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const int eb = dtype == PA_F32 ? 4 : 2;
+    cuuint64_t dims[3] = {(cuuint64_t)head_dim, (cuuint64_t)num_kv_heads, (cuuint64_t)rows};
+    cuuint64_t strides[2] = {(cuuint64_t)head_dim * eb, (cuuint64_t)head_dim * eb * num_kv_heads};
+    cuuint32_t box[3] = {(cuuint32_t)head_dim, (cuuint32_t)box_heads, (cuuint32_t)box_rows};
+    cuuint32_t estride[3] = {1, 1, 1};
+    CUresult r = fn(map, dt, 3, const_cast<void *>(base), dims, strides, box, estride,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
+}
+
+int device_sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return n;
+}
+
+}  // namespace pa

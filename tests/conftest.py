@@ -27,6 +27,13 @@ def oracle_mod():
 
 
 @pytest.fixture(scope="session")
+def pa_lib_path():
+    """Build libpa.so (if stale) through the entry point's builder and return its path."""
+    import __graft_entry__
+    return __graft_entry__._builder().build()
+
+
+@pytest.fixture(scope="session")
 def cuda_ok():
     import torch
     if not torch.cuda.is_available():

@@ -36,7 +36,8 @@ def gpu_step(case, out_dtype=torch.float32, device="cuda", status=None):
     q = case.query.to(device)
     out = torch.full(tuple(q.shape), float("nan"), dtype=out_dtype, device=device)
     if case.is_decode:
-        nbytes = pa.pa_decode_workspace_size(case.num_seqs, case.num_heads, case.head_dim,
+        nbytes = pa.pa_decode_workspace_size(case.num_seqs, case.num_heads, case.num_kv_heads,
+                                             case.head_dim,
                                              case.max_context_len)
         ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=device)
         pa.pa_decode(out, q, kc, vc, bt, cl, case.max_context_len, case.scale, workspace=ws,

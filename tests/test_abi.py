@@ -11,10 +11,8 @@ ROOT = Path(__file__).resolve().parents[1]
 
 
 @pytest.fixture(scope="module")
-def lib():
-    from paged_kv_attention_write_gb300 import build
-    path = build.build()
-    return ctypes.CDLL(str(path))
+def lib(pa_lib_path):
+    return ctypes.CDLL(str(pa_lib_path))
 
 
 def _declared_functions():
@@ -44,12 +42,14 @@ def test_status_strings_and_version(lib):
 
 def test_workspace_size_is_host_arithmetic(lib):
     lib.pa_decode_workspace_size.restype = ctypes.c_size_t
-    lib.pa_decode_workspace_size.argtypes = [ctypes.c_int] * 4
-    assert lib.pa_decode_workspace_size(0, 32, 128, 4096) == 0
-    short = lib.pa_decode_workspace_size(8, 32, 128, 100)
-    long = lib.pa_decode_workspace_size(8, 32, 128, 32768)
-    assert long > 0 and long >= short
-    assert long % 16 == 0
+    lib.pa_decode_workspace_size.argtypes = [ctypes.c_int] * 5
+    assert lib.pa_decode_workspace_size(0, 32, 8, 128, 4096) == 0
+    assert lib.pa_decode_workspace_size(8, 32, 8, 96, 4096) == 0      # unsupported head dim
+    assert lib.pa_decode_workspace_size(8, 24, 8, 128, 4096) == 0     # G = 3
+    small = lib.pa_decode_workspace_size(8, 32, 8, 128, 100)
+    big = lib.pa_decode_workspace_size(256, 32, 8, 128, 32768)
+    assert 0 < small < big
+    assert big % 16 == 0
 
 
 # Host-side validation: each call below must be rejected before anything runs.
@@ -72,8 +72,7 @@ def _decode(lib, **over):
     (dict(kvdt=7), -1), (dict(out_dtype=9), -1), (dict(S=-1), -1), (dict(query=None), -1),
     (dict(kc=FAKE + 4), -1), (dict(out=FAKE + 2), -1), (dict(cl=FAKE + 1), -1),
     (dict(scale=float("nan")), -1), (dict(maxctx=-5), -1),
-    (dict(maxctx=100000, ws=None), -3), (dict(maxctx=100000, wsb=16), -3),
-    (dict(maxctx=100000, ws=FAKE + 8), -3),
+    (dict(ws=None), -3), (dict(ws=FAKE + 8), -3), (dict(Hkv=6, Hq=12), -2),
 ])
 def test_decode_rejects_bad_arguments(lib, over, code):
     assert _decode(lib, **over) == code
