@@ -141,6 +141,34 @@ int pa_decode(void *out, pa_dtype out_dtype, const void *query, const void *key_
               pa_stream_t stream);
 
 /*
+ * pa_decode_noalloc -- pa_decode for callers that cannot allocate device
+ * memory: plugin hosts and serving runtimes that own all device memory and hand
+ * kernels only their tensors, hot paths where a cudaMalloc could synchronise
+ * the device, and language bindings without a device allocator.  The pages
+ * describe no such call; it exists only for these callers.
+ *
+ * Same arguments, results and error behaviour as pa_decode, without the
+ * workspace: the scratch lives in one static device array of
+ * PA_DECODE_NOALLOC_SCRATCH_BYTES inside the library (held by every GPU that
+ * loads the library until the process exits).  A problem whose scratch
+ * (pa_decode_workspace_size) exceeds it returns PA_ERR_WORKSPACE before
+ * anything runs; with 152 SMs, Hq = 32, Hkv = 8 and D = 128 that allows about 350
+ * sequences.  Nothing is allocated and nothing needs clearing between calls.
+ *
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress); make that first call before any stream capture.
+ * All calls on a device share the one array: two calls whose kernels overlap
+ * on the GPU (different streams, no ordering between them) race and corrupt
+ * each other's results.
+ */
+#define PA_DECODE_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
+int pa_decode_noalloc(void *out, pa_dtype out_dtype, const void *query, const void *key_cache,
+                      const void *value_cache, const int32_t *block_tables, int max_blocks_per_seq,
+                      const int32_t *context_lens, int max_context_len, int num_seqs, int num_heads,
+                      int num_kv_heads, int head_dim, int block_size, int num_blocks, float scale,
+                      pa_dtype kv_dtype, int32_t *status, pa_stream_t stream);
+
+/*
  * pa_prefill_chunk -- chunked-prefill attention.  Sequence s owns the packed
  * query rows query_start_loc[s] .. query_start_loc[s+1]-1 (Lq_s rows, the
  * newest tokens of the sequence, whose K/V are already in the cache).  Row i

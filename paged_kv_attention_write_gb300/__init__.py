@@ -23,7 +23,7 @@ from typing import Optional
 import torch
 
 __all__ = [
-    "PAError", "pa_reshape_and_cache", "pa_decode_workspace_size", "pa_decode",
+    "PAError", "pa_reshape_and_cache", "pa_decode_workspace_size", "pa_decode", "pa_decode_noalloc",
     "pa_prefill_chunk", "pa_copy_blocks", "pa_status_string", "pa_version", "library_path",
     "PA_F32", "PA_F16", "PA_BF16",
 ]
@@ -45,14 +45,16 @@ _lib.pa_decode_workspace_size.argtypes = [_i32, _i32, _i32, _i32, _i32]
 _lib.pa_decode_workspace_size.restype = _sz
 _lib.pa_decode.argtypes = [_vp, _i32, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32,
                            _i32, _i32, _f32, _i32, _vp, _sz, _vp, _vp]
+_lib.pa_decode_noalloc.argtypes = [_vp, _i32, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32,
+                                   _i32, _i32, _i32, _f32, _i32, _vp, _vp]
 _lib.pa_prefill_chunk.argtypes = [_vp, _i32, _vp, _vp, _i32, _i32, _vp, _vp, _vp, _i32, _vp, _i32,
                                   _i32, _i32, _i32, _i32, _i32, _i32, _f32, _i32, _vp, _vp]
 _lib.pa_copy_blocks.argtypes = [_vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _vp, _vp]
 _lib.pa_status_string.argtypes = [_i32]
 _lib.pa_status_string.restype = ctypes.c_char_p
 _lib.pa_version.argtypes = []
-for _name in ("pa_reshape_and_cache", "pa_decode", "pa_prefill_chunk", "pa_copy_blocks",
-              "pa_version"):
+for _name in ("pa_reshape_and_cache", "pa_decode", "pa_decode_noalloc", "pa_prefill_chunk",
+              "pa_copy_blocks", "pa_version"):
     getattr(_lib, _name).restype = _i32
 
 
@@ -125,6 +127,19 @@ def pa_decode(out, query, key_cache, value_cache, block_tables, context_lens, ma
                           int(max_context_len), S, Hq, Hkv, D, bs, NB, float(scale),
                           _dt(key_cache), _ptr(workspace), ws_bytes, _ptr(status),
                           _stream(stream)), "pa_decode")
+
+
+def pa_decode_noalloc(out, query, key_cache, value_cache, block_tables, context_lens,
+                      max_context_len: int, scale: float, *, status=None, stream=None) -> None:
+    """pa_decode with the library's static scratch instead of a caller workspace, for
+    callers that cannot allocate device memory.  Calls that overlap on the GPU race."""
+    S, Hq, D = query.shape
+    NB, bs, Hkv, _ = key_cache.shape
+    _check(_lib.pa_decode_noalloc(_ptr(out), _dt(out), _ptr(query), _ptr(key_cache),
+                                  _ptr(value_cache), _ptr(block_tables), block_tables.shape[1],
+                                  _ptr(context_lens), int(max_context_len), S, Hq, Hkv, D, bs, NB,
+                                  float(scale), _dt(key_cache), _ptr(status), _stream(stream)),
+           "pa_decode_noalloc")
 
 
 def pa_prefill_chunk(out, query, query_start_loc, max_query_len: int, key_cache, value_cache,
