@@ -79,22 +79,44 @@ def prefill_work(case) -> tuple[float, int]:
     return flops, byts
 
 
-def kernel_source_hash() -> str:
-    src = (ROOT / "paged_kv_attention_write_gb300" / "csrc" / "decode.cu").read_bytes()
-    return hashlib.sha256(src).hexdigest()[:16]
+def kernel_source_hash(kind: str = "decode") -> str:
+    """Hash of the CUDA sources a kernel is built from (ties ncu counters to a kernel version)."""
+    csrc = ROOT / "paged_kv_attention_write_gb300" / "csrc"
+    files = {"decode": ["decode.cu", "tma.cuh", "common.cuh"],
+             "prefill": ["prefill.cu", "common.cuh"]}[kind]
+    h = hashlib.sha256()
+    for f in files:
+        h.update((csrc / f).read_bytes())
+    return h.hexdigest()[:16]
 
 
-def profiled_traffic():
-    """DRAM bytes per decode launch from the committed ncu summary, if it was taken on the
-    current decode kernel source; else None."""
+def profiled_traffic(kind: str, workload: str):
+    """DRAM bytes (read + write) per launch from the committed ncu summary, if it was taken
+    on the current kernel sources and this workload; else None."""
     p = ROOT / "profiles" / "traffic.json"
     if not p.exists():
         return None
-    d = json.loads(p.read_text())
-    e = d.get("decode")
-    if not e or e.get("source_sha256_16") != kernel_source_hash():
+    e = json.loads(p.read_text()).get(kind, {}).get(workload)
+    if not e or e.get("source_sha256_16") != kernel_source_hash(kind):
         return None
     return e.get("dram_bytes_per_launch")
+
+
+class L2Flush:
+    """Between timed steps: write a buffer twice the L2 size, then read another one, so
+    that L2 holds neither the step's inputs nor dirty lines that the timed kernels would
+    have to write back.  Runs outside the CUDA-event pair of each step."""
+
+    def __init__(self, device):
+        l2 = torch.cuda.get_device_properties(device).L2_cache_size
+        n = max(2 * l2, 256 << 20)
+        self.w = torch.empty(n, dtype=torch.uint8, device=device)
+        self.r = torch.ones(n // 4, dtype=torch.int32, device=device)
+        self.sink = torch.empty((), dtype=torch.int64, device=device)
+
+    def __call__(self):
+        self.w.zero_()
+        torch.sum(self.r, dim=0, dtype=torch.int64, out=self.sink)
 
 
 class ClockSampler:
@@ -182,8 +204,22 @@ class DecodeStep:
                                              case.max_context_len)
         self.ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=device)
         self.max_ctx = case.max_context_len
-        # pinned host staging for the end-to-end measurement
-        self.h_in = {k: getattr(self, k).cpu().pin_memory() for k in ("q", "nk", "nv", "slots", "bt", "cl")}
+        # End-to-end staging: the step's inputs packed in one pinned host buffer and one
+        # device buffer (256-byte aligned fields), one copy each way per step.
+        names = ("q", "nk", "nv", "slots", "bt", "cl")
+        offs, total = {}, 0
+        for k in names:
+            t = getattr(self, k)
+            offs[k] = total
+            total += (t.numel() * t.element_size() + 255) // 256 * 256
+        self.h_in = torch.empty(total, dtype=torch.uint8).pin_memory()
+        self.d_in = torch.empty(total, dtype=torch.uint8, device=device)
+        self.e2e_views = {}
+        for k in names:
+            t = getattr(self, k)
+            nb = t.numel() * t.element_size()
+            self.h_in[offs[k]:offs[k] + nb].copy_(t.cpu().contiguous().view(-1).view(torch.uint8))
+            self.e2e_views[k] = self.d_in[offs[k]:offs[k] + nb].view(t.dtype).view(t.shape)
         self.h_out = torch.empty(self.out.shape, dtype=torch.float32).pin_memory()
 
     def reshape(self):
@@ -198,14 +234,17 @@ class DecodeStep:
         self.decode()
 
     def e2e_step(self):
-        """Host buffers in, host result out: H2D of the step inputs, the step, D2H."""
-        for k, h in self.h_in.items():
-            getattr(self, k).copy_(h, non_blocking=True)
-        self.step()
+        """Host buffers in, host result out: one H2D copy of the packed step inputs, the
+        step through the public API on the device copies, one D2H copy of the output."""
+        self.d_in.copy_(self.h_in, non_blocking=True)
+        v = self.e2e_views
+        self.pa.pa_reshape_and_cache(v["nk"], v["nv"], self.kc, self.vc, v["slots"])
+        self.pa.pa_decode(self.out, v["q"], self.kc, self.vc, v["bt"], v["cl"], self.max_ctx,
+                          self.case.scale, workspace=self.ws)
         self.h_out.copy_(self.out, non_blocking=True)
 
     def h2d_bytes(self):
-        return sum(t.numel() * t.element_size() for t in self.h_in.values())
+        return self.h_in.numel()
 
     def d2h_bytes(self):
         return self.h_out.numel() * self.h_out.element_size()
@@ -215,17 +254,128 @@ class DecodeStep:
         return 4
 
 
+class PrefillStep:
+    """Device-resident inputs of one chunked-prefill step: the chunk's K/V written to their
+    slots, then prefill attention of the chunk over prefix + chunk."""
+
+    def __init__(self, case, device):
+        import paged_kv_attention_write_gb300 as pa
+        self.pa = pa
+        self.case = case
+        self.kc = case.key_cache.to(device)
+        self.vc = case.value_cache.to(device)
+        self.bt = case.block_tables.to(device)
+        self.cl = case.context_lens.to(device)
+        self.q = case.query.to(device)
+        self.qsl = case.query_start_loc.to(device)
+        self.nk = case.new_key.to(device)
+        self.nv = case.new_value.to(device)
+        self.slots = case.slot_mapping.to(device)
+        self.out = torch.empty(tuple(case.query.shape), dtype=torch.float32, device=device)
+        self.mq = int((case.query_start_loc[1:] - case.query_start_loc[:-1]).max())
+        names = ("q", "nk", "nv", "slots", "bt", "cl", "qsl")
+        offs, total = {}, 0
+        for k in names:
+            t = getattr(self, k)
+            offs[k] = total
+            total += (t.numel() * t.element_size() + 255) // 256 * 256
+        self.h_in = torch.empty(total, dtype=torch.uint8).pin_memory()
+        self.d_in = torch.empty(total, dtype=torch.uint8, device=device)
+        self.e2e_views = {}
+        for k in names:
+            t = getattr(self, k)
+            nb = t.numel() * t.element_size()
+            self.h_in[offs[k]:offs[k] + nb].copy_(t.cpu().contiguous().view(-1).view(torch.uint8))
+            self.e2e_views[k] = self.d_in[offs[k]:offs[k] + nb].view(t.dtype).view(t.shape)
+        self.h_out = torch.empty(self.out.shape, dtype=torch.float32).pin_memory()
+
+    def prefill(self, v=None):
+        v = v or {"q": self.q, "qsl": self.qsl, "bt": self.bt, "cl": self.cl}
+        self.pa.pa_prefill_chunk(self.out, v["q"], v["qsl"], self.mq, self.kc, self.vc, v["bt"],
+                                 v["cl"], self.case.max_context_len, self.case.scale)
+
+    def step(self):
+        self.pa.pa_reshape_and_cache(self.nk, self.nv, self.kc, self.vc, self.slots)
+        self.prefill()
+
+    def e2e_step(self):
+        self.d_in.copy_(self.h_in, non_blocking=True)
+        v = self.e2e_views
+        self.pa.pa_reshape_and_cache(v["nk"], v["nv"], self.kc, self.vc, v["slots"])
+        self.prefill(v)
+        self.h_out.copy_(self.out, non_blocking=True)
+
+
+def prefill_arm(args, case, device, rank, world, dist_on):
+    """``--workload prefill_chunk``: the chunked-prefill row timed on its own."""
+    hbm_peak, tc_peak, peak_kind = peaks()
+    st = PrefillStep(case, device)
+    flush = L2Flush(device)
+    flops, byts = prefill_work(case)
+    for _ in range(args.warmup):
+        st.step()
+    torch.cuda.synchronize()
+    pf_ms, _ = time_steps(st.prefill, args.steps, flush, dist_on)
+    with ClockSampler(device.index) as clocks:
+        step_ms, wall = time_steps(st.step, args.steps, flush, dist_on)
+    e2e_ms, _ = time_steps(st.e2e_step, max(3, args.steps // 4), flush, dist_on)
+    ms_step = _max_over_ranks(statistics.mean(step_ms), dist_on)
+    ms_pf = _max_over_ranks(statistics.mean(pf_ms), dist_on)
+    ms_e2e = _max_over_ranks(statistics.mean(e2e_ms), dist_on)
+    if rank != 0:
+        return None
+    tfs = flops / (ms_pf * 1e-3) / 1e12
+    return {
+        "metric": "paged-attn chunked-prefill TFLOP/s (causal-exact FLOPs)",
+        "value": round(world * flops / (ms_step * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) q/k/v, shuffled block pool)",
+        "config": {"workload": case.name, "num_seqs": case.num_seqs,
+                   "prefix_lens": case.meta.get("prefix_lens"), "chunk_lens": case.meta.get("chunk_lens"),
+                   "block_size": case.block_size, "num_heads": case.num_heads,
+                   "num_kv_heads": case.num_kv_heads, "head_dim": case.head_dim,
+                   "flops_per_step": flops,
+                   "l2": "L2 flushed before each timed step (256 MB write, then 256 MB read of another buffer, outside the timed events)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "tokens_per_s": round(world * int(case.query.shape[0]) / (ms_step * 1e-3), 1),
+        "roofline": {"kernel": "pa_prefill_chunk", "bound": "tensor", "achieved": round(tfs, 1),
+                     "peak": tc_peak, "unit": "TFLOP/s", "frac": round(tfs / tc_peak, 4),
+                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json bf16_tflops, burst)",
+                     "traffic": profiled_traffic("prefill", args.workload),
+                     "algorithmic_bytes_per_launch": byts, "ms_per_launch": round(ms_pf, 5),
+                     "hbm_frac": round(byts / (ms_pf * 1e-3) / 1e9 / hbm_peak, 4)},
+        "e2e": {"value": round(world * flops / (ms_e2e * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                "ms_per_step": round(ms_e2e, 5), "h2d_bytes_per_step": st.h_in.numel(),
+                "d2h_bytes_per_step": st.h_out.numel() * 4},
+        "gpu_launches": args.steps * 2,
+        "clocks": clocks.summary(),
+        "timed_region_s": round(wall, 3),
+    }
+
+
 def _barrier(dist_on):
     if dist_on:
         torch.distributed.barrier()
 
 
 def _max_over_ranks(x: float, dist_on: bool) -> float:
+    """Slowest rank's time: a MAX all-reduce of one number (timing only, not the data path)."""
     if not dist_on:
         return x
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if torch.distributed.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
     return float(t.item())
+
+
+def shard_of(num_units: int, rank: int, world: int) -> range:
+    """Units of a sharded batch owned by ``rank`` (contiguous, sizes differ by at most 1).
+    The bench runs whole replicas per rank (weak scaling); a caller that splits one batch
+    of independent sequences over ranks takes this range of it, with no collective."""
+    lo = num_units * rank // world
+    hi = num_units * (rank + 1) // world
+    return range(lo, hi)
 
 
 def time_steps(fn, steps, flush, dist_on):
@@ -237,7 +387,7 @@ def time_steps(fn, steps, flush, dist_on):
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     for i in range(steps):
-        flush.zero_()
+        flush()
         starts[i].record()
         fn()
         ends[i].record()
@@ -254,10 +404,9 @@ def gpu_arm(args, rank, world, dist_on):
     hbm_peak, tc_peak, peak_kind = peaks()
     case = workloads.WORKLOADS[args.workload]()
     if not case.is_decode:
-        raise SystemExit("the headline bench times a decode workload")
+        return prefill_arm(args, case, device, rank, world, dist_on)
     st = DecodeStep(case, device)
-    l2 = torch.cuda.get_device_properties(device).L2_cache_size
-    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=device)
+    flush = L2Flush(device)
     byts = decode_bytes(case)
 
     for _ in range(args.warmup):
@@ -312,7 +461,7 @@ def gpu_arm(args, rank, world, dist_on):
             "num_kv_heads": case.num_kv_heads,
             "head_dim": case.head_dim,
             "kv_bytes_per_step": byts["kv"],
-            "l2": "inputs (0.8 GB of K/V) larger than L2, and L2 flushed (256 MB write) before each timed step",
+            "l2": "inputs larger than L2, and L2 flushed before each timed step (256 MB write, then 256 MB read of another buffer, outside the timed events)",
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
         },
         "seq_steps_per_s": round(world * case.num_seqs / (ms_step * 1e-3), 1),
@@ -326,7 +475,7 @@ def gpu_arm(args, rank, world, dist_on):
             "unit": "GB/s",
             "frac": round(dec_gbs / hbm_peak, 4),
             "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback",
-            "traffic": profiled_traffic(),
+            "traffic": profiled_traffic("decode", args.workload),
             "algorithmic_bytes_per_launch": byts["decode"],
             "ms_per_launch": round(ms_dec, 5),
         },
@@ -452,6 +601,8 @@ def reference_arm(args, rank, world, budget_s: float = 150.0):
         sub.slot_mapping = case.slot_mapping[:1]
         return sub
 
+    if not case.is_decode:
+        return reference_prefill(args, case, world)
     full = int(case.context_lens[0])
     probe = sample(min(full, 2048))
     t0 = time.perf_counter()
@@ -481,6 +632,57 @@ def reference_arm(args, rank, world, budget_s: float = 150.0):
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "kind": "oracle",
                          "cores": oracle.num_threads(), "sample": desc},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def reference_prefill(args, case, world, budget_s: float = 150.0):
+    """Reference arm on the prefill workload: the oracle on the first sequence's chunk,
+    its rows truncated so that the whole run takes about ``budget_s`` seconds."""
+    import oracle
+    kc, vc = case.key_cache.clone(), case.value_cache.clone()
+    oracle.reshape_and_cache(case.new_key, case.new_value, kc, vc, case.slot_mapping, case.block_size)
+    lq = int(case.query_start_loc[1] - case.query_start_loc[0])
+
+    def sub_case(rows):
+        sub = workloads.PagedCase(**{**case.__dict__})
+        sub.query = case.query[lq - rows:lq].contiguous()  # the chunk's last rows
+        sub.query_start_loc = torch.tensor([0, rows], dtype=torch.int32)
+        sub.block_tables = case.block_tables[:1]
+        sub.context_lens = case.context_lens[:1]
+        return sub
+
+    def run(sub):
+        return oracle.paged_attention(sub.query, sub.query_start_loc, kc, vc, sub.block_tables,
+                                      sub.context_lens, case.scale)
+
+    probe = sub_case(min(lq, 8))
+    t0 = time.perf_counter()
+    run(probe)
+    per_row = (time.perf_counter() - t0) / int(probe.query.shape[0])
+    rows = int(max(1, min(lq, budget_s / (args.steps + args.warmup) / max(per_row, 1e-9))))
+    sub = sub_case(rows)
+    flops, _ = prefill_work(sub)
+    for _ in range(args.warmup):
+        run(sub)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        run(sub)
+        times.append(time.perf_counter() - t0)
+    t = statistics.mean(times)
+    value = flops / t / 1e12
+    desc = f"last {rows} of the first sequence's {lq} chunk rows, all heads, per step"
+    return {
+        "impl": "reference", "metric": "paged-attn chunked-prefill TFLOP/s (causal-exact FLOPs)",
+        "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(t * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) q/k/v, shuffled block pool)",
+        "config": {"workload": case.name, "sample": desc},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "kind": "oracle",
+                         "cores": oracle.num_threads(), "sample": desc},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
     }
 
 
