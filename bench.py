@@ -111,12 +111,12 @@ class L2Flush:
         l2 = torch.cuda.get_device_properties(device).L2_cache_size
         n = max(2 * l2, 256 << 20)
         self.w = torch.empty(n, dtype=torch.uint8, device=device)
-        self.r = torch.ones(n // 4, dtype=torch.int32, device=device)
-        self.sink = torch.empty((), dtype=torch.int64, device=device)
+        self.r = torch.ones(n // 4, dtype=torch.float32, device=device)
+        self.sink = torch.empty((), dtype=torch.float32, device=device)
 
     def __call__(self):
         self.w.zero_()
-        torch.sum(self.r, dim=0, dtype=torch.int64, out=self.sink)
+        torch.sum(self.r, dim=0, out=self.sink)
 
 
 class ClockSampler:
