@@ -1,4 +1,5 @@
-// prefill.cu -- chunked-prefill paged attention on the tensor cores.
+// prefill.cu -- chunked-prefill paged attention on the 5th-generation tensor
+// cores (tcgen05: operands in shared memory via TMA, accumulators in TMEM).
 //
 // A chunk of Lq query tokens per sequence (the newest tokens, whose K/V the
 // caller already wrote into the cache) attends the sequence's keys gathered
@@ -8,91 +9,141 @@
 // under a token budget, 512 tokens per chunk); TensorSharp "Mistral 3" page,
 // section 11 (paged K/V gather, then fused attention).
 //
-// Grid (query tile, kv head, sequence).  A query tile is 64 rows of
-// (token, head) pairs of ONE kv head's G query heads, so every K/V tile
-// gathered into shared memory serves G heads.  Four warps own 16 rows each.
-// Per 64-key tile: S = Q K^T and O += P V with mma.sync m16n8k16 (fp32
-// accumulate), online softmax in registers in the log2 domain, cp.async
-// double buffering of the gathered K/V rows (zero-filled past the context).
-#include "common.cuh"
+// Grid (query tile, kv head, sequence).  A query tile is 128 rows of
+// (token, head) pairs of ONE kv head's G query heads (128/G tokens), so each
+// gathered K/V tile serves G heads.  Per 128-key tile j:
+//   S_j = Q K_j^T   tcgen05.mma M128 N128 K=D, fp32 in TMEM (two buffers)
+//   P_j             one thread per row reads its S row from TMEM: mask,
+//                   online softmax in the log2 domain with lazy rescaling
+//                   (the reference max moves only when a score exceeds it by
+//                   2^8), P_j rounded to bf16/fp16 into shared memory
+//   O  += P_j V_j   tcgen05.mma M128 N=D K128, fp32 in TMEM; V is the
+//                   MN-major operand
+// Warp roles: warp 0 issues the TMA loads (the Q tile once; per key tile one
+// 3-D box per block of K and of V through the block table, two stages),
+// warp 1 issues the MMAs, warps 2-5 run the softmax and the epilogue.  All
+// operand tiles use the 128-byte swizzle.  Every wait is an mbarrier wait
+// bounded in time.
+#include <type_traits>
+
+#include "tma.cuh"
 
 namespace pa {
 namespace {
 
-constexpr int kPfWarps = 4;
-constexpr int kPfThreads = kPfWarps * 32;
-constexpr int kBM = 64;  // query rows per CTA (16 per warp)
-constexpr int kBN = 64;  // keys per tile
+constexpr int kPfThreads = 6 * 32;
+constexpr int kBM = 128;  // query rows per CTA
+constexpr int kBN = 128;  // keys per tile
+constexpr float kRescaleLog2 = 8.f;
+
+// ---------------------------------------------------------------- tcgen05 helpers
+// Shared-memory matrix descriptor (sm_100 format): start address, leading and
+// stride byte offsets (>> 4), version 1, 128-byte swizzle.  K-major operands:
+// SBO = 1024 (between 8-row groups), the start advances 32 bytes per 16-element
+// k step inside the swizzle span.  MN-major operands: LBO = bytes between
+// 64-element atoms along MN, SBO = 1024 (between 8-row groups along K).
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFF);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFF) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFF) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
+// Instruction descriptor of kind::f16 with fp32 accumulation, A K-major.
+__host__ __device__ constexpr uint32_t mma_idesc(int M, int N, bool bf16, bool b_mn_major) {
+    return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) |
+           ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_f16(uint32_t tmem_d, uint64_t da, uint64_t db, uint32_t idesc,
+                                        uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+        "l"(da), "l"(db), "r"(idesc), "r"(accumulate));
+}
+
+// The mbarrier completes one arrival when every MMA issued so far has finished.
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// 32 lanes x 32 consecutive 32-bit TMEM columns <-> 32 registers per thread.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+          "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+          "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+        "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+        "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
+        "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
+        "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// Generic-proxy shared-memory writes become visible to the tensor core (async proxy).
+__device__ __forceinline__ void fence_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+                 : "memory");
+}
 
 template <class T>
-struct MmaType;
+__device__ __forceinline__ uint32_t pack2(float lo, float hi);
 template <>
-struct MmaType<F16> {
-    static __device__ __forceinline__ void mma(float (&d)[4], const uint32_t (&a)[4],
-                                               uint32_t b0, uint32_t b1) {
-        asm volatile(
-            "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-            "{%8,%9}, {%0,%1,%2,%3};"
-            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-    }
-    static __device__ __forceinline__ uint32_t pack(float lo, float hi) {
-        __half2 h = __floats2half2_rn(lo, hi);
-        return *reinterpret_cast<uint32_t *>(&h);
-    }
-};
+__device__ __forceinline__ uint32_t pack2<BF16>(float lo, float hi) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
 template <>
-struct MmaType<BF16> {
-    static __device__ __forceinline__ void mma(float (&d)[4], const uint32_t (&a)[4],
-                                               uint32_t b0, uint32_t b1) {
-        asm volatile(
-            "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-            "{%8,%9}, {%0,%1,%2,%3};"
-            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-    }
-    static __device__ __forceinline__ uint32_t pack(float lo, float hi) {
-        __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
-        return *reinterpret_cast<uint32_t *>(&h);
-    }
-};
-
-__device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], uint32_t addr) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(addr));
+__device__ __forceinline__ uint32_t pack2<F16>(float lo, float hi) {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
 }
-__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t (&r)[4], uint32_t addr) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(addr));
+// Sum of a packed pair as it enters the P.V product (numerator and denominator agree).
+template <class T>
+__device__ __forceinline__ float unpack_sum(uint32_t u);
+template <>
+__device__ __forceinline__ float unpack_sum<BF16>(uint32_t u) {
+    return __uint_as_float(u << 16) + __uint_as_float(u & 0xffff0000u);
 }
-// 16-byte async copy; src_bytes == 0 zero-fills the destination.
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, int src_bytes) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
-                 "r"(src_bytes));
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N));
-}
-
-// Shared-memory tile of R rows x D 16-bit elements; the 16-byte chunk c of row
-// `row` is stored at chunk c ^ (row % 8) so that ldmatrix's 8-row phases hit
-// distinct banks.
-template <int D>
-__device__ __forceinline__ uint32_t swz(uint32_t base, int row, int chunk) {
-    return base + (uint32_t)(row * (D * 2) + ((chunk ^ (row & 7)) << 4));
+template <>
+__device__ __forceinline__ float unpack_sum<F16>(uint32_t u) {
+    const float2 f = __half22float2(*reinterpret_cast<__half2 *>(&u));
+    return f.x + f.y;
 }
 
 struct PrefillParams {
     void *out;
     pa_dtype out_dtype;
-    const void *query;
     const int32_t *query_start_loc;
-    const void *key_cache;
-    const void *value_cache;
     const int32_t *block_tables;
     const int32_t *context_lens;
     int max_blocks_per_seq, num_heads, num_kv_heads, block_size, num_blocks, max_context_len;
@@ -101,33 +152,76 @@ struct PrefillParams {
     int32_t *status;
 };
 
-template <class OutT>
-__device__ __forceinline__ void store2(void *out, int64_t idx, float a, float b) {
-    store_out(static_cast<OutT *>(out) + idx, a, b);
-}
+template <int D>
+struct PfShape {
+    static constexpr int HALVES = D / 64;                    // 128-byte swizzle atoms along D
+    static constexpr int Q_BYTES = kBM * D * 2;              // [half][128 rows][128 B]
+    static constexpr int KV_BYTES = kBN * D * 2;             // K (and V) per stage, same layout
+    static constexpr int P_BYTES = kBM * kBN * 2;            // [2 key halves][128 rows][128 B]
+    static constexpr int OFF_Q = 0;
+    static constexpr int OFF_KV = OFF_Q + Q_BYTES;           // 2 stages x [K | V]
+    static constexpr int OFF_P = OFF_KV + 2 * 2 * KV_BYTES;  // 2 buffers
+    static constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
+    static constexpr int SMEM = 1024 + OFF_BAR + 256;
+    static_assert(SMEM <= 227 * 1024, "shared memory budget");
+};
+
+// TMEM: two S buffers (128 columns each) and O (D columns).
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmemS0 = 0, kTmemO = 256;
 
 template <class T, int D, int G>
-__global__ void __launch_bounds__(kPfThreads)
-prefill_kernel(const PrefillParams p) {
-    constexpr int TT = kBM / G;        // query tokens per tile
-    constexpr int CH = D / 8;          // 16-byte chunks per row
-    constexpr int KS = D / 16;         // k-steps over the head dim
-    constexpr int NTS = kBN / 8;       // n-tiles of S per warp
-    constexpr int NTO = D / 8;         // n-tiles of O per warp
-    using Elt = typename T::storage;
-    using M = MmaType<T>;
+__global__ void __launch_bounds__(kPfThreads, 1)
+prefill_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
+                  const __grid_constant__ CUtensorMap vmap, const PrefillParams p) {
+    using Sh = PfShape<D>;
+    constexpr int TT = kBM / G;  // query tokens per tile
+    constexpr int KSTEPS_S = D / 16, KSTEPS_PV = kBN / 16;
+    constexpr bool kBf16 = std::is_same<T, BF16>::value;
+    constexpr uint32_t IDESC_S = mma_idesc(128, kBN, kBf16, false);
+    constexpr uint32_t IDESC_PV = mma_idesc(128, D, kBf16, true);
 
-    extern __shared__ __align__(128) unsigned char smem[];
-    const uint32_t sQ = (uint32_t)__cvta_generic_to_shared(smem);
-    const uint32_t sK0 = sQ + kBM * D * 2;
-    const uint32_t sV0 = sK0 + 2 * kBN * D * 2;
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *smem = reinterpret_cast<unsigned char *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t sQ = sbase + Sh::OFF_Q, sKV = sbase + Sh::OFF_KV, sP = sbase + Sh::OFF_P;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Sh::OFF_BAR);
+    const uint32_t b0 = smem_u32(bars);
+    const uint32_t bar_q = b0;
+    auto bar_kv_full = [&](int i) { return b0 + 8 * (1 + i); };   // TMA bytes landed
+    auto bar_kv_empty = [&](int i) { return b0 + 8 * (3 + i); };  // K and V of the stage consumed
+    auto bar_s_full = [&](int i) { return b0 + 8 * (5 + i); };    // S buffer written
+    auto bar_s_free = [&](int i) { return b0 + 8 * (7 + i); };    // S buffer read by the softmax
+    auto bar_p_full = [&](int i) { return b0 + 8 * (9 + i); };    // P buffer written
+    auto bar_pv_done = [&](int i) { return b0 + 8 * (11 + i); };  // P.V of that buffer finished
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 13);
+    int *abort_flag = reinterpret_cast<int *>(bars + 14);
 
-    pdl_wait_previous();
-    pdl_launch_dependents();
+    const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
     const int g = blockIdx.y, s = blockIdx.z;
     const int qt = gridDim.x - 1 - blockIdx.x;  // heaviest (latest) tiles first
-    const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
-    const int Hq = p.num_heads, Hkv = p.num_kv_heads, bs = p.block_size;
+    const int Hq = p.num_heads, bs = p.block_size;
+
+    // ---- prologue independent of earlier kernels
+    if (tid == 0) {
+        *abort_flag = 0;
+        mbar_init(bar_q, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar_kv_full(i), 1);
+            mbar_init(bar_kv_empty(i), 1);
+            mbar_init(bar_s_full(i), 1);
+            mbar_init(bar_s_free(i), 4);
+            mbar_init(bar_p_full(i), 4);
+            mbar_init(bar_pv_done(i), 1);
+        }
+        fence_barrier_init();
+        prefetch_tensormap(&qmap);
+        prefetch_tensormap(&kmap);
+        prefetch_tensormap(&vmap);
+    }
+    pdl_wait_previous();
+    pdl_launch_dependents();
 
     const int q0 = p.query_start_loc[s];
     const int Lq = p.query_start_loc[s + 1] - q0;
@@ -145,220 +239,277 @@ prefill_kernel(const PrefillParams p) {
     }
     const int tok_begin = qt * TT;
     const int tok_end = min(Lq, tok_begin + TT);
-    const int pos0 = C - Lq;                        // absolute position of chunk row 0
-    const int kv_end = pos0 + tok_end;              // keys visible to the tile's last row
+    const int pos0 = C - Lq;                 // absolute position of chunk row 0
+    const int kv_end = pos0 + tok_end;       // keys visible to the tile's last row
     const int n_tiles = (kv_end + kBN - 1) / kBN;
-
-    const Elt *kc = static_cast<const Elt *>(p.key_cache);
-    const Elt *vc = static_cast<const Elt *>(p.value_cache);
     const int32_t *bt = p.block_tables + (int64_t)s * p.max_blocks_per_seq;
-    const int64_t slot_stride = (int64_t)Hkv * D;
 
-    // ---- Q tile: row r = (token tok_begin + r / G, head g*G + r % G)
-    {
-        const Elt *qbase = static_cast<const Elt *>(p.query);
-        for (int i = tid; i < kBM * CH; i += kPfThreads) {
-            const int row = i / CH, ch = i % CH;
-            const int tok = tok_begin + row / G;
-            const bool ok = tok < Lq;
-            const Elt *src = qbase + ((int64_t)(q0 + (ok ? tok : 0)) * Hq + g * G + row % G) * D + ch * 8;
-            cp_async16(swz<D>(sQ, row, ch), src, ok ? 16 : 0);
-        }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(tmem_slot)),
+                     "r"(kTmemCols));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
     }
-    // ---- K/V tile loader: 64 gathered key rows, zero past the context or on a bad block id
-    auto load_kv = [&](int tile, int buf) {
-        const int k0 = tile * kBN;
-        const uint32_t sK = sK0 + buf * kBN * D * 2, sV = sV0 + buf * kBN * D * 2;
-        for (int i = tid; i < kBN * CH; i += kPfThreads) {
-            const int row = i / CH, ch = i % CH;
-            const int j = k0 + row;
-            int64_t off = 0;
-            int bytes = 0;
-            if (j < C) {
-                const int blk = bt[j / bs];
-                if (blk >= 0 && blk < p.num_blocks) {
-                    off = ((int64_t)blk * bs + j % bs) * slot_stride + g * D + ch * 8;
-                    bytes = 16;
-                } else if (ch == 0) {
-                    report(p.status, PA_DEVERR_BLOCK_ID);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    volatile int *abort_v = abort_flag;
+
+    if (warp == 0) {
+        // ============================================ producer (TMA)
+        if (lane == 0) {
+            const uint64_t policy = policy_evict_first();
+            // Q: tokens [tok_begin, +TT) x heads [g*G, +G) x one D half per box
+            mbar_expect_tx(bar_q, Sh::Q_BYTES);
+            for (int hf = 0; hf < Sh::HALVES; ++hf)
+                tma_load_3d(sQ + hf * (kBM * 128), &qmap, hf * 64, g * G, q0 + tok_begin, bar_q, policy);
+            mbar_arrive(bar_q);
+            const uint32_t box_bytes = (uint32_t)bs * 128;  // one block of one kv head, one D half
+            for (int j = 0; j < n_tiles; ++j) {
+                const int st = j & 1;
+                if (*abort_v || !mbar_wait(bar_kv_empty(st), ((j >> 1) & 1) ^ 1, p.status)) {
+                    *abort_v = 1;
+                    break;
+                }
+                const uint32_t sK = sKV + st * 2 * Sh::KV_BYTES, sV = sK + Sh::KV_BYTES;
+                const int k0 = j * kBN;
+#pragma unroll 1
+                for (int b = 0; b < kBN / bs; ++b) {
+                    const int key = k0 + b * bs;
+                    if (key >= kv_end) break;
+                    const int id = bt[key / bs];
+                    if (id < 0 || id >= p.num_blocks) {  // never dereferenced
+                        report(p.status, PA_DEVERR_BLOCK_ID);
+                        continue;
+                    }
+                    mbar_expect_tx(bar_kv_full(st), 2 * Sh::HALVES * box_bytes);
+                    for (int hf = 0; hf < Sh::HALVES; ++hf) {
+                        const uint32_t off = hf * (kBN * 128) + b * box_bytes;
+                        tma_load_3d(sK + off, &kmap, hf * 64, g, id * bs, bar_kv_full(st), policy);
+                        tma_load_3d(sV + off, &vmap, hf * 64, g, id * bs, bar_kv_full(st), policy);
+                    }
+                }
+                mbar_arrive(bar_kv_full(st));
+            }
+        }
+    } else if (warp == 1) {
+        // ============================================ MMA issuer
+        if (lane == 0) {
+            bool ok = mbar_wait(bar_q, 0, p.status);
+            auto pv = [&](int t) {  // O += P_t V_t
+                const int pb = t & 1;
+                if (!ok || !mbar_wait(bar_p_full(pb), (t >> 1) & 1, p.status)) {
+                    ok = false;
+                    return;
+                }
+                tc_fence_after();
+                const uint32_t sV = sKV + pb * 2 * Sh::KV_BYTES + Sh::KV_BYTES;
+                const uint32_t sPb = sP + pb * Sh::P_BYTES;
+#pragma unroll
+                for (int kk = 0; kk < KSTEPS_PV; ++kk) {
+                    const uint64_t da = smem_desc(sPb + (kk / 4) * (kBM * 128) + (kk % 4) * 32, 16, 1024);
+                    const uint64_t db = smem_desc(sV + kk * 16 * 128, kBN * 128, 1024);
+                    mma_f16(tmem + kTmemO, da, db, IDESC_PV, (t > 0 || kk > 0) ? 1u : 0u);
+                }
+                mma_commit(bar_pv_done(pb));
+                mma_commit(bar_kv_empty(pb));
+            };
+            for (int j = 0; j < n_tiles && ok; ++j) {
+                const int st = j & 1;
+                ok = !*abort_v && mbar_wait(bar_kv_full(st), (j >> 1) & 1, p.status);
+                if (ok && j >= 2) ok = mbar_wait(bar_s_free(st), ((j - 2) >> 1) & 1, p.status);
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t sK = sKV + st * 2 * Sh::KV_BYTES;
+#pragma unroll
+                for (int ks = 0; ks < KSTEPS_S; ++ks) {
+                    const uint32_t off = (ks / 4) * (kBM * 128) + (ks % 4) * 32;
+                    const uint64_t da = smem_desc(sQ + off, 16, 1024);
+                    const uint64_t db = smem_desc(sK + off, 16, 1024);
+                    mma_f16(tmem + kTmemS0 + st * kBN, da, db, IDESC_S, ks > 0 ? 1u : 0u);
+                }
+                mma_commit(bar_s_full(st));
+                if (j >= 1) pv(j - 1);
+            }
+            if (ok) pv(n_tiles - 1);
+            if (!ok) *abort_v = 1;
+        }
+    } else {
+        // ============================================ softmax (one thread per query row)
+        const int quarter = warp & 3;            // TMEM lanes this warp may access
+        const int row = quarter * 32 + lane;     // query row of the tile
+        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+        // rows past the chunk (a ragged last tile) are computed but never stored; they
+        // see exactly the keys that were loaded
+        const int pos = min(pos0 + tok_begin + row / G, kv_end - 1);
+        float m_ref = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int j = 0; j < n_tiles; ++j) {
+            const int sb = j & 1;
+            ok = ok && !*abort_v && mbar_wait(bar_s_full(sb), (j >> 1) & 1, p.status);
+            if (!ok) {
+                *abort_v = 1;
+                break;
+            }
+            tc_fence_after();
+            const int k0 = j * kBN;
+            float sv[kBN];
+#pragma unroll
+            for (int c0 = 0; c0 < kBN; c0 += 32) {
+                uint32_t r[32];
+                tmem_ld32(tmem + lane_off + kTmemS0 + sb * kBN + c0, r);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) sv[c0 + i] = __uint_as_float(r[i]);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_s_free(sb));  // the S buffer may be overwritten
+            // mask (keys k0 .. k0+lim-1 are visible) and row max, log2 domain
+            const int lim = min(pos + 1, C) - k0;
+            float mx = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < kBN; ++c) {
+                const float v = c < lim ? sv[c] * p.qk_scale_log2 : -INFINITY;
+                sv[c] = v;
+                mx = fmaxf(mx, v);
+            }
+            // lazy rescale; warp-uniform because the O row is read and written by the
+            // whole warp (tcgen05.ld / st)
+            const bool grow = mx > m_ref + kRescaleLog2;
+            if (__any_sync(kFullMask, grow)) {
+                const float m_new = grow ? mx : m_ref;
+                const float alpha = m_new == m_ref ? 1.f : exp2f(m_ref - m_new);  // 0 from -inf
+                l *= alpha;
+                m_ref = m_new;
+                if (j >= 1) {  // O holds tiles < j: wait for the last P.V, then scale the row
+                    ok = ok && mbar_wait(bar_pv_done((j - 1) & 1), ((j - 1) >> 1) & 1, p.status);
+                    tc_fence_after();
+#pragma unroll
+                    for (int c0 = 0; c0 < D; c0 += 32) {
+                        uint32_t r[32];
+                        tmem_ld32(tmem + lane_off + kTmemO + c0, r);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+                        tmem_st32(tmem + lane_off + kTmemO + c0, r);
+                    }
+                    tmem_wait_st();
                 }
             }
-            cp_async16(swz<D>(sK, row, ch), kc + off, bytes);
-            cp_async16(swz<D>(sV, row, ch), vc + off, bytes);
-        }
-    };
-    load_kv(0, 0);
-    cp_async_commit();
-
-    // Rows this thread holds in the accumulator fragments.
-    const int row_a = warp * 16 + lane / 4;
-    const int pos_a = pos0 + tok_begin + row_a / G;
-    const int pos_b = pos0 + tok_begin + (row_a + 8) / G;
-
-    uint32_t qa[KS][4];
-    float o[NTO][4];
+            // the P buffer sb was read by the P.V of tile j-2
+            if (j >= 2) ok = ok && mbar_wait(bar_pv_done(sb), ((j - 2) >> 1) & 1, p.status);
+            // P row: 128 keys as 16 chunks of 8 (16 B), two 64-key halves, 128-byte swizzle
+            const uint32_t prow = sP + sb * Sh::P_BYTES + row * 128;
+            float rs = 0.f;
 #pragma unroll
-    for (int n = 0; n < NTO; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-    float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.f, l_b = 0.f;
-
-    for (int tile = 0; tile < n_tiles; ++tile) {
-        const int buf = tile & 1;
-        if (tile + 1 < n_tiles) load_kv(tile + 1, buf ^ 1);
-        cp_async_commit();
-        cp_async_wait<1>();
-        __syncthreads();
-        if (tile == 0) {
+            for (int ch = 0; ch < kBN / 8; ++ch) {
+                uint32_t w[4];
 #pragma unroll
-            for (int ks = 0; ks < KS; ++ks) {
-                const int m = lane / 8;
-                const int row = warp * 16 + (m % 2) * 8 + lane % 8;
-                ldmatrix_x4(qa[ks], swz<D>(sQ, row, ks * 2 + m / 2));
-            }
-        }
-        const uint32_t sK = sK0 + buf * kBN * D * 2, sV = sV0 + buf * kBN * D * 2;
-        // ---- S = Q K^T (16 rows x 64 keys per warp)
-        float sc[NTS][4];
-#pragma unroll
-        for (int n = 0; n < NTS; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
-#pragma unroll
-        for (int n = 0; n < NTS; ++n) {
-#pragma unroll
-            for (int ks = 0; ks < KS; ks += 2) {
-                uint32_t b[4];
-                const int m = lane / 8;
-                ldmatrix_x4(b, swz<D>(sK, n * 8 + lane % 8, ks * 2 + m));
-                M::mma(sc[n], qa[ks], b[0], b[1]);
-                M::mma(sc[n], qa[ks + 1], b[2], b[3]);
-            }
-        }
-        // ---- mask, online softmax (log2 domain)
-        const int k0 = tile * kBN;
-        const bool need_mask = k0 + kBN - 1 > pos0 + tok_begin + warp * 16 / G || k0 + kBN > C;
-        float mx_a = -INFINITY, mx_b = -INFINITY;
-#pragma unroll
-        for (int n = 0; n < NTS; ++n) {
-#pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                const int j = k0 + n * 8 + (lane % 4) * 2 + c;
-                float sa = sc[n][c] * p.qk_scale_log2;
-                float sb = sc[n][2 + c] * p.qk_scale_log2;
-                if (need_mask) {
-                    if (j > pos_a || j >= C) sa = -INFINITY;
-                    if (j > pos_b || j >= C) sb = -INFINITY;
+                for (int i = 0; i < 4; ++i) {
+                    w[i] = pack2<T>(exp2f(sv[ch * 8 + 2 * i] - m_ref), exp2f(sv[ch * 8 + 2 * i + 1] - m_ref));
+                    rs += unpack_sum<T>(w[i]);
                 }
-                sc[n][c] = sa;
-                sc[n][2 + c] = sb;
-                mx_a = fmaxf(mx_a, sa);
-                mx_b = fmaxf(mx_b, sb);
+                sts128(prow + (ch / 8) * (kBM * 128) + (((ch % 8) ^ (row & 7)) << 4), w[0], w[1], w[2], w[3]);
+            }
+            l += rs;
+            // keys past kv_end in this tile (not loaded, or past the context): zero V rows,
+            // so that 0-weight rows never meet stale or NaN data
+            if (k0 + kBN > kv_end) {
+                const int valid = kv_end - k0;
+                ok = ok && mbar_wait(bar_kv_full(sb), (j >> 1) & 1, p.status);
+                const uint32_t sV = sKV + sb * 2 * Sh::KV_BYTES + Sh::KV_BYTES;
+                for (int i = tid - 64; i < (kBN - valid) * Sh::HALVES * 8; i += 128) {
+                    const int rr = valid + i / (Sh::HALVES * 8), rest = i % (Sh::HALVES * 8);
+                    sts128(sV + (rest / 8) * (kBN * 128) + rr * 128 + (rest % 8) * 16, 0u, 0u, 0u, 0u);
+                }
+            }
+            fence_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_p_full(sb));
+        }
+        // ---- epilogue: O / l for the rows of this chunk
+        const int last = n_tiles - 1;
+        if (ok) ok = mbar_wait(bar_pv_done(last & 1), (last >> 1) & 1, p.status);
+        tc_fence_after();
+        const int tok = tok_begin + row / G;
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        const int64_t orow = ((int64_t)(q0 + tok) * Hq + g * G + row % G) * D;
+#pragma unroll
+        for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t r[32];
+            tmem_ld32(tmem + lane_off + kTmemO + c0, r);
+            tmem_wait_ld();
+            if (ok && tok < Lq) {
+                if (p.out_dtype == PA_F32) {
+                    float4 *o = reinterpret_cast<float4 *>(static_cast<float *>(p.out) + orow + c0);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        o[i] = make_float4(__uint_as_float(r[4 * i]) * inv, __uint_as_float(r[4 * i + 1]) * inv,
+                                           __uint_as_float(r[4 * i + 2]) * inv, __uint_as_float(r[4 * i + 3]) * inv);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const float a = __uint_as_float(r[2 * i]) * inv, b = __uint_as_float(r[2 * i + 1]) * inv;
+                        if (p.out_dtype == PA_F16)
+                            store_out(static_cast<__half *>(p.out) + orow + c0 + 2 * i, a, b);
+                        else
+                            store_out(static_cast<__nv_bfloat16 *>(p.out) + orow + c0 + 2 * i, a, b);
+                    }
+                }
             }
         }
-#pragma unroll
-        for (int off = 1; off < 4; off <<= 1) {
-            mx_a = fmaxf(mx_a, __shfl_xor_sync(kFullMask, mx_a, off));
-            mx_b = fmaxf(mx_b, __shfl_xor_sync(kFullMask, mx_b, off));
-        }
-        const float mn_a = fmaxf(m_a, mx_a), mn_b = fmaxf(m_b, mx_b);
-        const float base_a = mn_a == -INFINITY ? 0.f : mn_a;
-        const float base_b = mn_b == -INFINITY ? 0.f : mn_b;
-        const float al_a = exp2f(m_a - base_a), al_b = exp2f(m_b - base_b);
-        m_a = mn_a;
-        m_b = mn_b;
-        float rs_a = 0.f, rs_b = 0.f;
-        uint32_t pa[NTS][2];
-#pragma unroll
-        for (int n = 0; n < NTS; ++n) {
-            const float p0 = exp2f(sc[n][0] - base_a), p1 = exp2f(sc[n][1] - base_a);
-            const float p2 = exp2f(sc[n][2] - base_b), p3 = exp2f(sc[n][3] - base_b);
-            rs_a += p0 + p1;
-            rs_b += p2 + p3;
-            pa[n][0] = M::pack(p0, p1);
-            pa[n][1] = M::pack(p2, p3);
-        }
-        l_a = l_a * al_a + rs_a;
-        l_b = l_b * al_b + rs_b;
-#pragma unroll
-        for (int n = 0; n < NTO; ++n) {
-            o[n][0] *= al_a;
-            o[n][1] *= al_a;
-            o[n][2] *= al_b;
-            o[n][3] *= al_b;
-        }
-        // ---- O += P V
-#pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk) {
-            const uint32_t a[4] = {pa[2 * kk][0], pa[2 * kk][1], pa[2 * kk + 1][0], pa[2 * kk + 1][1]};
-#pragma unroll
-            for (int n = 0; n < NTO; n += 2) {
-                uint32_t b[4];
-                const int m = lane / 8;
-                ldmatrix_x4_trans(b, swz<D>(sV, kk * 16 + (m % 2) * 8 + lane % 8, n + m / 2));
-                M::mma(o[n], a, b[0], b[1]);
-                M::mma(o[n + 1], a, b[2], b[3]);
-            }
-        }
-        __syncthreads();  // this buffer is refilled two tiles later
     }
-    cp_async_wait<0>();
-
-    // ---- row sums across the quad, normalise, store
-#pragma unroll
-    for (int off = 1; off < 4; off <<= 1) {
-        l_a += __shfl_xor_sync(kFullMask, l_a, off);
-        l_b += __shfl_xor_sync(kFullMask, l_b, off);
-    }
-    const float inv_a = l_a > 0.f ? 1.f / l_a : 0.f, inv_b = l_b > 0.f ? 1.f / l_b : 0.f;
-    const int tok_a = tok_begin + row_a / G, tok_b = tok_begin + (row_a + 8) / G;
-    const int64_t oa = ((int64_t)(q0 + tok_a) * Hq + g * G + row_a % G) * D;
-    const int64_t ob = ((int64_t)(q0 + tok_b) * Hq + g * G + (row_a + 8) % G) * D;
-#pragma unroll
-    for (int n = 0; n < NTO; ++n) {
-        const int d = n * 8 + (lane % 4) * 2;
-        if (tok_a < Lq) {
-            if (p.out_dtype == PA_F32) store2<float>(p.out, oa + d, o[n][0] * inv_a, o[n][1] * inv_a);
-            else if (p.out_dtype == PA_F16) store2<__half>(p.out, oa + d, o[n][0] * inv_a, o[n][1] * inv_a);
-            else store2<__nv_bfloat16>(p.out, oa + d, o[n][0] * inv_a, o[n][1] * inv_a);
-        }
-        if (tok_b < Lq) {
-            if (p.out_dtype == PA_F32) store2<float>(p.out, ob + d, o[n][2] * inv_b, o[n][3] * inv_b);
-            else if (p.out_dtype == PA_F16) store2<__half>(p.out, ob + d, o[n][2] * inv_b, o[n][3] * inv_b);
-            else store2<__nv_bfloat16>(p.out, ob + d, o[n][2] * inv_b, o[n][3] * inv_b);
-        }
+    // ---- teardown: every TMEM access has completed before the columns are released
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
     }
 }
 
 template <class T, int D, int G>
-int launch_typed(const PrefillParams &prm, int max_query_len, int num_seqs, cudaStream_t st) {
+int launch_typed(const PrefillParams &prm, const CUtensorMap &qm, const CUtensorMap &km,
+                 const CUtensorMap &vm, int max_query_len, int num_seqs, cudaStream_t st) {
     constexpr int TT = kBM / G;
-    const int smem = (kBM + 4 * kBN) * D * 2;
-    static bool configured = false;  // attribute set once per process (per instantiation)
-    if (!configured) {
-        if (cudaFuncSetAttribute(prefill_kernel<T, D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    const int smem = PfShape<D>::SMEM;
+    static int configured_device = -1;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (configured_device != dev) {
+        if (cudaFuncSetAttribute(prefill_tc_kernel<T, D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  smem) != cudaSuccess)
             return PA_ERR_CUDA;
-        configured = true;
+        configured_device = dev;
     }
     dim3 grid((max_query_len + TT - 1) / TT, prm.num_kv_heads, num_seqs);
-    return launch_pdl(prefill_kernel<T, D, G>, grid, dim3(kPfThreads), smem, st, prm) == cudaSuccess
+    return launch_pdl(prefill_tc_kernel<T, D, G>, grid, dim3(kPfThreads), smem, st, qm, km, vm, prm) ==
+                   cudaSuccess
                ? PA_OK
                : PA_ERR_CUDA;
 }
 
 template <class T, int D>
-int dispatch_g(const PrefillParams &prm, int G, int mq, int S, cudaStream_t st) {
+int dispatch_g(const PrefillParams &prm, int G, const CUtensorMap &qm, const CUtensorMap &km,
+               const CUtensorMap &vm, int mq, int S, cudaStream_t st) {
     switch (G) {
-        case 1: return launch_typed<T, D, 1>(prm, mq, S, st);
-        case 2: return launch_typed<T, D, 2>(prm, mq, S, st);
-        case 4: return launch_typed<T, D, 4>(prm, mq, S, st);
-        case 8: return launch_typed<T, D, 8>(prm, mq, S, st);
+        case 1: return launch_typed<T, D, 1>(prm, qm, km, vm, mq, S, st);
+        case 2: return launch_typed<T, D, 2>(prm, qm, km, vm, mq, S, st);
+        case 4: return launch_typed<T, D, 4>(prm, qm, km, vm, mq, S, st);
+        case 8: return launch_typed<T, D, 8>(prm, qm, km, vm, mq, S, st);
         default: return PA_ERR_UNSUPPORTED;
     }
 }
 
 template <class T>
-int dispatch_d(const PrefillParams &prm, int D, int G, int mq, int S, cudaStream_t st) {
+int dispatch_d(const PrefillParams &prm, int D, int G, const CUtensorMap &qm, const CUtensorMap &km,
+               const CUtensorMap &vm, int mq, int S, cudaStream_t st) {
     switch (D) {
-        case 64: return dispatch_g<T, 64>(prm, G, mq, S, st);
-        case 128: return dispatch_g<T, 128>(prm, G, mq, S, st);
+        case 64: return dispatch_g<T, 64>(prm, G, qm, km, vm, mq, S, st);
+        case 128: return dispatch_g<T, 128>(prm, G, qm, km, vm, mq, S, st);
         default: return PA_ERR_UNSUPPORTED;
     }
 }
@@ -370,10 +521,7 @@ int launch_prefill(const PrefillArgs &a) {
     PrefillParams prm{};
     prm.out = a.out;
     prm.out_dtype = a.out_dtype;
-    prm.query = a.query;
     prm.query_start_loc = a.query_start_loc;
-    prm.key_cache = a.key_cache;
-    prm.value_cache = a.value_cache;
     prm.block_tables = a.block_tables;
     prm.context_lens = a.context_lens;
     prm.max_blocks_per_seq = a.max_blocks_per_seq;
@@ -386,9 +534,22 @@ int launch_prefill(const PrefillArgs &a) {
     prm.qk_scale_log2 = a.scale * kLog2e;
     prm.status = a.status;
     const int G = a.num_heads / a.num_kv_heads;
+    const int64_t pool_rows = (int64_t)a.num_blocks * a.block_size;
+    if (pool_rows <= 0 || pool_rows > INT32_MAX) return PA_ERR_INVALID_ARG;
+    // Boxes are 64 elements (128 bytes, the swizzle span) wide along D.  Q boxes
+    // cover the G heads of one kv head for 128/G tokens; K/V boxes one block of
+    // one kv head.
+    CUtensorMap qm, km, vm;
+    if (make_tensor_map_3d(&qm, a.query, a.kv_dtype, a.head_dim, a.num_heads, a.num_tokens, 64, G,
+                           kBM / G, true) != PA_OK ||
+        make_tensor_map_3d(&km, a.key_cache, a.kv_dtype, a.head_dim, a.num_kv_heads, pool_rows, 64, 1,
+                           a.block_size, true) != PA_OK ||
+        make_tensor_map_3d(&vm, a.value_cache, a.kv_dtype, a.head_dim, a.num_kv_heads, pool_rows, 64, 1,
+                           a.block_size, true) != PA_OK)
+        return PA_ERR_CUDA;
     switch (a.kv_dtype) {
-        case PA_F16: return dispatch_d<F16>(prm, a.head_dim, G, a.max_query_len, a.num_seqs, a.stream);
-        case PA_BF16: return dispatch_d<BF16>(prm, a.head_dim, G, a.max_query_len, a.num_seqs, a.stream);
+        case PA_F16: return dispatch_d<F16>(prm, a.head_dim, G, qm, km, vm, a.max_query_len, a.num_seqs, a.stream);
+        case PA_BF16: return dispatch_d<BF16>(prm, a.head_dim, G, qm, km, vm, a.max_query_len, a.num_seqs, a.stream);
         default: return PA_ERR_UNSUPPORTED;
     }
 }

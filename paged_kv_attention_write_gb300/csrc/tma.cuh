@@ -104,6 +104,12 @@ __device__ __forceinline__ void named_barrier(int id, int threads) {
 int make_kv_tensor_map(CUtensorMap *map, const void *base, pa_dtype dtype, int head_dim,
                        int num_kv_heads, int64_t rows, int box_heads, int box_rows);
 
+// General 3-D tensor map [dim2][dim1][dim0] (dim0 innermost, dense) with box
+// {box0, box1, box2}; 128-byte swizzle when asked (box0 * element size must then
+// be at most 128 bytes).
+int make_tensor_map_3d(CUtensorMap *map, const void *base, pa_dtype dtype, int dim0, int dim1,
+                       int64_t dim2, int box0, int box1, int box2, bool swizzle128);
+
 // Streaming multiprocessors of the current device (0 if none can be queried).
 int device_sm_count();
 

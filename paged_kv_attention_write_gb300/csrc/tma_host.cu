@@ -22,22 +22,29 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 }  // namespace
 
-int make_kv_tensor_map(CUtensorMap *map, const void *base, pa_dtype dtype, int head_dim,
-                       int num_kv_heads, int64_t rows, int box_heads, int box_rows) {
+int make_tensor_map_3d(CUtensorMap *map, const void *base, pa_dtype dtype, int dim0, int dim1,
+                       int64_t dim2, int box0, int box1, int box2, bool swizzle128) {
     auto fn = encode_fn();
     if (!fn) return PA_ERR_CUDA;
     CUtensorMapDataType dt = dtype == PA_F32   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
                              : dtype == PA_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
                                                : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     const int eb = dtype == PA_F32 ? 4 : 2;
-    cuuint64_t dims[3] = {(cuuint64_t)head_dim, (cuuint64_t)num_kv_heads, (cuuint64_t)rows};
-    cuuint64_t strides[2] = {(cuuint64_t)head_dim * eb, (cuuint64_t)head_dim * eb * num_kv_heads};
-    cuuint32_t box[3] = {(cuuint32_t)head_dim, (cuuint32_t)box_heads, (cuuint32_t)box_rows};
+    cuuint64_t dims[3] = {(cuuint64_t)dim0, (cuuint64_t)dim1, (cuuint64_t)dim2};
+    cuuint64_t strides[2] = {(cuuint64_t)dim0 * eb, (cuuint64_t)dim0 * eb * dim1};
+    cuuint32_t box[3] = {(cuuint32_t)box0, (cuuint32_t)box1, (cuuint32_t)box2};
     cuuint32_t estride[3] = {1, 1, 1};
     CUresult r = fn(map, dt, 3, const_cast<void *>(base), dims, strides, box, estride,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
+}
+
+int make_kv_tensor_map(CUtensorMap *map, const void *base, pa_dtype dtype, int head_dim,
+                       int num_kv_heads, int64_t rows, int box_heads, int box_rows) {
+    return make_tensor_map_3d(map, base, dtype, head_dim, num_kv_heads, rows, head_dim, box_heads,
+                              box_rows, false);
 }
 
 int device_sm_count() {
