@@ -89,6 +89,14 @@ __device__ __forceinline__ uint4 ldg_stream(const void *p) {
     return v;
 }
 
+// 2^x with the hardware approximation (ex2.approx.ftz: relative error ~2^-22, flushes
+// subnormal results to zero); the softmax weights need nothing more precise.
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 __device__ __forceinline__ void report(int32_t *status, int bit) {
     if (status) atomicOr(status, bit);
 }

@@ -547,7 +547,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
 #pragma unroll
                 for (int o = 1; o < 32; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(kFullMask, mx, o));
                 const float mn = fmaxf(m[hh], mx);
-                const float alpha = exp2f(m[hh] - mn);  // 0 while m is -inf
+                const float alpha = fast_exp2(m[hh] - mn);  // 0 while m is -inf
                 m[hh] = mn;
                 const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
@@ -563,7 +563,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
         // ---- weights of this lane's scores, shared through the warp's score buffer
 #pragma unroll
         for (int u = 0; u < R; ++u) {
-            const float e = exp2f(sc[u] - mref[u]);
+            const float e = fast_exp2(sc[u] - mref[u]);
             if (owner) l_lane[u] += e;
             wsc[tl_own * G + hb + u] = e;
         }
@@ -639,7 +639,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
             float L = 0.f, o0 = 0.f, o1 = 0.f;
             for (int j = 0; j < nsub; ++j) {
                 const int w = j * HG + hk;
-                const float f = exp2f(red_m[w * G + hh] - M);  // 0 for a slice without tokens
+                const float f = fast_exp2(red_m[w * G + hh] - M);  // 0 for a slice without tokens
                 L = fmaf(red_l[w * G + hh], f, L);
                 o0 = fmaf(red_o[(w * G + hh) * D + d], f, o0);
                 o1 = fmaf(red_o[(w * G + hh) * D + d + 1], f, o1);
@@ -733,13 +733,13 @@ __global__ void __launch_bounds__(D / 2) decode_reduce_kernel(const DecodeParams
         float bm = M;
 #pragma unroll
         for (int i = 0; i < kReduceBatch; ++i) bm = fmaxf(bm, mj[i]);
-        const float a = exp2f(M - bm);  // 0 on the first batch
+        const float a = fast_exp2(M - bm);  // 0 on the first batch
         L *= a;
         o0 *= a;
         o1 *= a;
 #pragma unroll
         for (int i = 0; i < kReduceBatch; ++i) {
-            const float f = exp2f(mj[i] - bm);  // 0 for padding entries
+            const float f = fast_exp2(mj[i] - bm);  // 0 for padding entries
             L = fmaf(lj[i], f, L);
             o0 = fmaf(oj[i].x, f, o0);
             o1 = fmaf(oj[i].y, f, o1);

@@ -16,14 +16,16 @@
 //   P_j             one thread per row reads its S row from TMEM: mask,
 //                   online softmax in the log2 domain with lazy rescaling
 //                   (the reference max moves only when a score exceeds it by
-//                   2^8), P_j rounded to bf16/fp16 into shared memory
-//   O  += P_j V_j   tcgen05.mma M128 N=D K128, fp32 in TMEM; V is the
-//                   MN-major operand
-// Warp roles: warp 0 issues the TMA loads (the Q tile once; per key tile one
-// 3-D box per block of K and of V through the block table, two stages),
-// warp 1 issues the MMAs, warps 2-5 run the softmax and the epilogue.  All
-// operand tiles use the 128-byte swizzle.  Every wait is an mbarrier wait
-// bounded in time.
+//                   2^8), P_j rounded to bf16/fp16 and written back to TMEM
+//   O  += P_j V_j   tcgen05.mma M128 N=D K128 with A = P from TMEM, fp32 in
+//                   TMEM; V is the MN-major shared-memory operand
+// Warp roles: warps 0 and 6 issue the TMA loads (the Q tile once; per key tile
+// one 3-D box per block through the block table, issued by the lanes in
+// parallel, into separate 3-stage K and V rings: a K stage frees when its S
+// finishes, a V stage when its P.V does), warp 1 issues the MMAs, warps 2-5
+// run the softmax and the epilogue.  All
+// shared-memory operands use the 128-byte swizzle.  Every wait is an mbarrier
+// wait bounded in time.
 #include <type_traits>
 
 #include "tma.cuh"
@@ -31,7 +33,7 @@
 namespace pa {
 namespace {
 
-constexpr int kPfThreads = 6 * 32;
+constexpr int kPfThreads = 7 * 32;
 constexpr int kBM = 128;  // query rows per CTA
 constexpr int kBN = 128;  // keys per tile
 constexpr float kRescaleLog2 = 8.f;
@@ -64,6 +66,16 @@ __device__ __forceinline__ void mma_f16(uint32_t tmem_d, uint64_t da, uint64_t d
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
         "l"(da), "l"(db), "r"(idesc), "r"(accumulate));
+}
+
+// Same, with A (M x 16 elements) read from TMEM: row i in lane i, two 16-bit
+// elements per 32-bit column, 8 columns per k step.
+__device__ __forceinline__ void mma_f16_tmem_a(uint32_t tmem_d, uint32_t tmem_a, uint64_t db,
+                                               uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem_d),
+        "r"(tmem_a), "l"(db), "r"(idesc), "r"(accumulate));
 }
 
 // The mbarrier completes one arrival when every MMA issued so far has finished.
@@ -154,27 +166,29 @@ struct PrefillParams {
 
 template <int D>
 struct PfShape {
-    static constexpr int HALVES = D / 64;                    // 128-byte swizzle atoms along D
-    static constexpr int Q_BYTES = kBM * D * 2;              // [half][128 rows][128 B]
-    static constexpr int KV_BYTES = kBN * D * 2;             // K (and V) per stage, same layout
-    static constexpr int P_BYTES = kBM * kBN * 2;            // [2 key halves][128 rows][128 B]
+    static constexpr int HALVES = D / 64;             // 128-byte swizzle atoms along D
+    static constexpr int Q_BYTES = kBM * D * 2;       // [half][128 rows][128 B]
+    static constexpr int KV_BYTES = kBN * D * 2;      // one K (or V) stage, same layout
+    static constexpr int NST = 3;                     // K stages and V stages
     static constexpr int OFF_Q = 0;
-    static constexpr int OFF_KV = OFF_Q + Q_BYTES;           // 2 stages x [K | V]
-    static constexpr int OFF_P = OFF_KV + 2 * 2 * KV_BYTES;  // 2 buffers
-    static constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
+    static constexpr int OFF_K = OFF_Q + Q_BYTES;
+    static constexpr int OFF_V = OFF_K + NST * KV_BYTES;
+    static constexpr int OFF_BAR = OFF_V + NST * KV_BYTES;
     static constexpr int SMEM = 1024 + OFF_BAR + 256;
     static_assert(SMEM <= 227 * 1024, "shared memory budget");
 };
 
-// TMEM: two S buffers (128 columns each) and O (D columns).
+// TMEM columns: S (fp32, 128 keys) in two buffers, O (fp32, D), P (two bf16/fp16 keys
+// per column, 128 keys) in two buffers.
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemS0 = 0, kTmemO = 256;
+constexpr uint32_t kTmemS0 = 0, kTmemO = 256, kTmemP0 = 384;
 
 template <class T, int D, int G>
 __global__ void __launch_bounds__(kPfThreads, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                   const __grid_constant__ CUtensorMap vmap, const PrefillParams p) {
     using Sh = PfShape<D>;
+    constexpr int NST = Sh::NST;
     constexpr int TT = kBM / G;  // query tokens per tile
     constexpr int KSTEPS_S = D / 16, KSTEPS_PV = kBN / 16;
     constexpr bool kBf16 = std::is_same<T, BF16>::value;
@@ -185,18 +199,21 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
     unsigned char *smem = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
-    const uint32_t sQ = sbase + Sh::OFF_Q, sKV = sbase + Sh::OFF_KV, sP = sbase + Sh::OFF_P;
+    const uint32_t sQ = sbase + Sh::OFF_Q, sK0 = sbase + Sh::OFF_K, sV0 = sbase + Sh::OFF_V;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Sh::OFF_BAR);
     const uint32_t b0 = smem_u32(bars);
     const uint32_t bar_q = b0;
-    auto bar_kv_full = [&](int i) { return b0 + 8 * (1 + i); };   // TMA bytes landed
-    auto bar_kv_empty = [&](int i) { return b0 + 8 * (3 + i); };  // K and V of the stage consumed
-    auto bar_s_full = [&](int i) { return b0 + 8 * (5 + i); };    // S buffer written
-    auto bar_s_free = [&](int i) { return b0 + 8 * (7 + i); };    // S buffer read by the softmax
-    auto bar_p_full = [&](int i) { return b0 + 8 * (9 + i); };    // P buffer written
-    auto bar_pv_done = [&](int i) { return b0 + 8 * (11 + i); };  // P.V of that buffer finished
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 13);
-    int *abort_flag = reinterpret_cast<int *>(bars + 14);
+    auto bar_k_full = [&](int i) { return b0 + 8 * (1 + i); };            // K stage landed
+    auto bar_k_empty = [&](int i) { return b0 + 8 * (1 + NST + i); };     // S of that K finished
+    auto bar_v_full = [&](int i) { return b0 + 8 * (1 + 2 * NST + i); };  // V stage landed
+    auto bar_v_empty = [&](int i) { return b0 + 8 * (1 + 3 * NST + i); }; // P.V of that V finished
+    constexpr int B2 = 1 + 4 * NST;
+    auto bar_s_full = [&](int i) { return b0 + 8 * (B2 + i); };      // S buffer written
+    auto bar_s_free = [&](int i) { return b0 + 8 * (B2 + 2 + i); };  // S buffer read by the softmax
+    auto bar_p_full = [&](int i) { return b0 + 8 * (B2 + 4 + i); };  // P buffer written
+    auto bar_pv_done = [&](int i) { return b0 + 8 * (B2 + 6 + i); }; // P.V of that P finished
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + B2 + 8);
+    int *abort_flag = reinterpret_cast<int *>(bars + B2 + 9);
 
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
     const int g = blockIdx.y, s = blockIdx.z;
@@ -207,9 +224,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
     if (tid == 0) {
         *abort_flag = 0;
         mbar_init(bar_q, 1);
+        for (int i = 0; i < NST; ++i) {
+            mbar_init(bar_k_full(i), 1);
+            mbar_init(bar_k_empty(i), 1);
+            mbar_init(bar_v_full(i), 1);
+            mbar_init(bar_v_empty(i), 1);
+        }
         for (int i = 0; i < 2; ++i) {
-            mbar_init(bar_kv_full(i), 1);
-            mbar_init(bar_kv_empty(i), 1);
             mbar_init(bar_s_full(i), 1);
             mbar_init(bar_s_free(i), 4);
             mbar_init(bar_p_full(i), 4);
@@ -256,80 +277,93 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
     const uint32_t tmem = *tmem_slot;
     volatile int *abort_v = abort_flag;
 
-    if (warp == 0) {
-        // ============================================ producer (TMA)
-        if (lane == 0) {
-            const uint64_t policy = policy_evict_first();
-            // Q: tokens [tok_begin, +TT) x heads [g*G, +G) x one D half per box
+    if (warp == 0 || warp == 6) {
+        // ============================================ producers (TMA): warp 0 loads K, warp 6 V
+        // A K stage frees when its S finishes, a V stage when its P.V does; each warp
+        // runs ahead on its own ring.  Lane b fetches the block id of the tile's b-th
+        // block two tiles ahead and issues that block's boxes; lane 0 posts the
+        // tile's transaction bytes first and arrives after the warp has issued.
+        const bool is_k = warp == 0;
+        const CUtensorMap *map = is_k ? &kmap : &vmap;
+        const uint32_t ring = is_k ? sK0 : sV0;
+        const uint64_t policy = policy_evict_first();
+        const int nb = kBN / bs;  // blocks per key tile (4, 8 or 16)
+        const uint32_t box_bytes = (uint32_t)bs * 128;  // one block of one kv head, one D half
+        auto block_id = [&](int j) {
+            const int key = j * kBN + lane * bs;
+            return (lane < nb && j < n_tiles && key < kv_end) ? bt[key / bs] : -1;
+        };
+        if (is_k && lane == 0) {  // Q: tokens [tok_begin, +TT) x heads [g*G, +G), one D half per box
             mbar_expect_tx(bar_q, Sh::Q_BYTES);
             for (int hf = 0; hf < Sh::HALVES; ++hf)
                 tma_load_3d(sQ + hf * (kBM * 128), &qmap, hf * 64, g * G, q0 + tok_begin, bar_q, policy);
             mbar_arrive(bar_q);
-            const uint32_t box_bytes = (uint32_t)bs * 128;  // one block of one kv head, one D half
-            for (int j = 0; j < n_tiles; ++j) {
-                const int st = j & 1;
-                if (*abort_v || !mbar_wait(bar_kv_empty(st), ((j >> 1) & 1) ^ 1, p.status)) {
-                    *abort_v = 1;
-                    break;
-                }
-                const uint32_t sK = sKV + st * 2 * Sh::KV_BYTES, sV = sK + Sh::KV_BYTES;
-                const int k0 = j * kBN;
-#pragma unroll 1
-                for (int b = 0; b < kBN / bs; ++b) {
-                    const int key = k0 + b * bs;
-                    if (key >= kv_end) break;
-                    const int id = bt[key / bs];
-                    if (id < 0 || id >= p.num_blocks) {  // never dereferenced
-                        report(p.status, PA_DEVERR_BLOCK_ID);
-                        continue;
-                    }
-                    mbar_expect_tx(bar_kv_full(st), 2 * Sh::HALVES * box_bytes);
-                    for (int hf = 0; hf < Sh::HALVES; ++hf) {
-                        const uint32_t off = hf * (kBN * 128) + b * box_bytes;
-                        tma_load_3d(sK + off, &kmap, hf * 64, g, id * bs, bar_kv_full(st), policy);
-                        tma_load_3d(sV + off, &vmap, hf * 64, g, id * bs, bar_kv_full(st), policy);
-                    }
-                }
-                mbar_arrive(bar_kv_full(st));
+        }
+        int id0 = block_id(0), id1 = block_id(1);
+        for (int j = 0; j < n_tiles; ++j) {
+            const int my_id = id0;
+            id0 = id1;
+            id1 = block_id(j + 2);
+            const int st = j % NST;
+            const uint32_t empty = is_k ? bar_k_empty(st) : bar_v_empty(st);
+            const uint32_t full = is_k ? bar_k_full(st) : bar_v_full(st);
+            int ok = 1;
+            if (lane == 0) ok = !*abort_v && mbar_wait(empty, ((j / NST) & 1) ^ 1, p.status);
+            if (!__shfl_sync(kFullMask, ok, 0)) {
+                if (lane == 0) *abort_v = 1;
+                break;
             }
+            const bool in_range = lane < nb && j * kBN + lane * bs < kv_end;
+            const bool valid = in_range && my_id >= 0 && my_id < p.num_blocks;
+            if (in_range && !valid) report(p.status, PA_DEVERR_BLOCK_ID);  // never dereferenced
+            const unsigned mine = __ballot_sync(kFullMask, valid);
+            if (lane == 0) mbar_expect_tx(full, __popc(mine) * Sh::HALVES * box_bytes);
+            __syncwarp();
+            if (valid) {
+                const uint32_t dst = ring + st * Sh::KV_BYTES + lane * box_bytes;
+                for (int hf = 0; hf < Sh::HALVES; ++hf)
+                    tma_load_3d(dst + hf * (kBN * 128), map, hf * 64, g, my_id * bs, full, policy);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(full);
         }
     } else if (warp == 1) {
         // ============================================ MMA issuer
         if (lane == 0) {
             bool ok = mbar_wait(bar_q, 0, p.status);
-            auto pv = [&](int t) {  // O += P_t V_t
-                const int pb = t & 1;
-                if (!ok || !mbar_wait(bar_p_full(pb), (t >> 1) & 1, p.status)) {
+            auto pv = [&](int t) {  // O += P_t V_t, P from TMEM
+                const int pb = t & 1, st = t % NST;
+                if (!ok || !mbar_wait(bar_v_full(st), (t / NST) & 1, p.status) ||
+                    !mbar_wait(bar_p_full(pb), (t >> 1) & 1, p.status)) {
                     ok = false;
                     return;
                 }
                 tc_fence_after();
-                const uint32_t sV = sKV + pb * 2 * Sh::KV_BYTES + Sh::KV_BYTES;
-                const uint32_t sPb = sP + pb * Sh::P_BYTES;
+                const uint32_t sV = sV0 + st * Sh::KV_BYTES;
 #pragma unroll
                 for (int kk = 0; kk < KSTEPS_PV; ++kk) {
-                    const uint64_t da = smem_desc(sPb + (kk / 4) * (kBM * 128) + (kk % 4) * 32, 16, 1024);
                     const uint64_t db = smem_desc(sV + kk * 16 * 128, kBN * 128, 1024);
-                    mma_f16(tmem + kTmemO, da, db, IDESC_PV, (t > 0 || kk > 0) ? 1u : 0u);
+                    mma_f16_tmem_a(tmem + kTmemO, tmem + kTmemP0 + pb * (kBN / 2) + kk * 8, db, IDESC_PV,
+                                   (t > 0 || kk > 0) ? 1u : 0u);
                 }
                 mma_commit(bar_pv_done(pb));
-                mma_commit(bar_kv_empty(pb));
+                mma_commit(bar_v_empty(st));
             };
             for (int j = 0; j < n_tiles && ok; ++j) {
-                const int st = j & 1;
-                ok = !*abort_v && mbar_wait(bar_kv_full(st), (j >> 1) & 1, p.status);
-                if (ok && j >= 2) ok = mbar_wait(bar_s_free(st), ((j - 2) >> 1) & 1, p.status);
+                const int st = j % NST, sb = j & 1;
+                ok = !*abort_v && mbar_wait(bar_k_full(st), (j / NST) & 1, p.status);
+                if (ok && j >= 2) ok = mbar_wait(bar_s_free(sb), ((j - 2) >> 1) & 1, p.status);
                 if (!ok) break;
                 tc_fence_after();
-                const uint32_t sK = sKV + st * 2 * Sh::KV_BYTES;
+                const uint32_t sK = sK0 + st * Sh::KV_BYTES;
 #pragma unroll
                 for (int ks = 0; ks < KSTEPS_S; ++ks) {
                     const uint32_t off = (ks / 4) * (kBM * 128) + (ks % 4) * 32;
-                    const uint64_t da = smem_desc(sQ + off, 16, 1024);
-                    const uint64_t db = smem_desc(sK + off, 16, 1024);
-                    mma_f16(tmem + kTmemS0 + st * kBN, da, db, IDESC_S, ks > 0 ? 1u : 0u);
+                    mma_f16(tmem + kTmemS0 + sb * kBN, smem_desc(sQ + off, 16, 1024),
+                            smem_desc(sK + off, 16, 1024), IDESC_S, ks > 0 ? 1u : 0u);
                 }
-                mma_commit(bar_s_full(st));
+                mma_commit(bar_s_full(sb));
+                mma_commit(bar_k_empty(st));
                 if (j >= 1) pv(j - 1);
             }
             if (ok) pv(n_tiles - 1);
@@ -343,6 +377,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
         // rows past the chunk (a ragged last tile) are computed but never stored; they
         // see exactly the keys that were loaded
         const int pos = min(pos0 + tok_begin + row / G, kv_end - 1);
+        const int row0_pos = pos0 + tok_begin;  // position of the tile's first row
         float m_ref = -INFINITY, l = 0.f;
         bool ok = true;
         for (int j = 0; j < n_tiles; ++j) {
@@ -355,32 +390,46 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
             tc_fence_after();
             const int k0 = j * kBN;
             float sv[kBN];
-#pragma unroll
-            for (int c0 = 0; c0 < kBN; c0 += 32) {
-                uint32_t r[32];
-                tmem_ld32(tmem + lane_off + kTmemS0 + sb * kBN + c0, r);
+            {
+                uint32_t r0[32], r1[32], r2[32], r3[32];
+                const uint32_t sa = tmem + lane_off + kTmemS0 + sb * kBN;
+                tmem_ld32(sa, r0);
+                tmem_ld32(sa + 32, r1);
+                tmem_ld32(sa + 64, r2);
+                tmem_ld32(sa + 96, r3);
                 tmem_wait_ld();
 #pragma unroll
-                for (int i = 0; i < 32; ++i) sv[c0 + i] = __uint_as_float(r[i]);
+                for (int i = 0; i < 32; ++i) {
+                    sv[i] = __uint_as_float(r0[i]);
+                    sv[32 + i] = __uint_as_float(r1[i]);
+                    sv[64 + i] = __uint_as_float(r2[i]);
+                    sv[96 + i] = __uint_as_float(r3[i]);
+                }
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_s_free(sb));  // the S buffer may be overwritten
-            // mask (keys k0 .. k0+lim-1 are visible) and row max, log2 domain
+            // mask (keys k0 .. k0+lim-1 are visible; only the last tiles need it) and row
+            // max of the raw scores, in eight independent chains
             const int lim = min(pos + 1, C) - k0;
-            float mx = -INFINITY;
+            if (k0 + kBN > row0_pos + 1 || k0 + kBN > C) {  // tile-uniform
 #pragma unroll
-            for (int c = 0; c < kBN; ++c) {
-                const float v = c < lim ? sv[c] * p.qk_scale_log2 : -INFINITY;
-                sv[c] = v;
-                mx = fmaxf(mx, v);
+                for (int c = 0; c < kBN; ++c) sv[c] = c < lim ? sv[c] : -INFINITY;
             }
+            float mx8[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) mx8[i] = sv[i];
+#pragma unroll
+            for (int c = 8; c < kBN; ++c) mx8[c % 8] = fmaxf(mx8[c % 8], sv[c]);
+            const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                   fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) *
+                             p.qk_scale_log2;
             // lazy rescale; warp-uniform because the O row is read and written by the
             // whole warp (tcgen05.ld / st)
             const bool grow = mx > m_ref + kRescaleLog2;
             if (__any_sync(kFullMask, grow)) {
                 const float m_new = grow ? mx : m_ref;
-                const float alpha = m_new == m_ref ? 1.f : exp2f(m_ref - m_new);  // 0 from -inf
+                const float alpha = m_new == m_ref ? 1.f : fast_exp2(m_ref - m_new);  // 0 from -inf
                 l *= alpha;
                 m_ref = m_new;
                 if (j >= 1) {  // O holds tiles < j: wait for the last P.V, then scale the row
@@ -400,32 +449,34 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
             }
             // the P buffer sb was read by the P.V of tile j-2
             if (j >= 2) ok = ok && mbar_wait(bar_pv_done(sb), ((j - 2) >> 1) & 1, p.status);
-            // P row: 128 keys as 16 chunks of 8 (16 B), two 64-key halves, 128-byte swizzle
-            const uint32_t prow = sP + sb * Sh::P_BYTES + row * 128;
-            float rs = 0.f;
+            // P row: 128 keys packed two per TMEM column
+            const float sc = p.qk_scale_log2, neg_m = -m_ref;
+            float rs4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int ch = 0; ch < kBN / 8; ++ch) {
-                uint32_t w[4];
+            for (int half = 0; half < 2; ++half) {
+                uint32_t w[32];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    w[i] = pack2<T>(exp2f(sv[ch * 8 + 2 * i] - m_ref), exp2f(sv[ch * 8 + 2 * i + 1] - m_ref));
-                    rs += unpack_sum<T>(w[i]);
+                for (int i = 0; i < 32; ++i) {
+                    const int c = half * 64 + 2 * i;
+                    w[i] = pack2<T>(fast_exp2(fmaf(sv[c], sc, neg_m)), fast_exp2(fmaf(sv[c + 1], sc, neg_m)));
+                    rs4[i & 3] += unpack_sum<T>(w[i]);
                 }
-                sts128(prow + (ch / 8) * (kBM * 128) + (((ch % 8) ^ (row & 7)) << 4), w[0], w[1], w[2], w[3]);
+                tmem_st32(tmem + lane_off + kTmemP0 + sb * (kBN / 2) + half * 32, w);
             }
-            l += rs;
+            tmem_wait_st();
+            l += (rs4[0] + rs4[1]) + (rs4[2] + rs4[3]);
             // keys past kv_end in this tile (not loaded, or past the context): zero V rows,
             // so that 0-weight rows never meet stale or NaN data
             if (k0 + kBN > kv_end) {
-                const int valid = kv_end - k0;
-                ok = ok && mbar_wait(bar_kv_full(sb), (j >> 1) & 1, p.status);
-                const uint32_t sV = sKV + sb * 2 * Sh::KV_BYTES + Sh::KV_BYTES;
+                const int valid = kv_end - k0, st = j % NST;
+                ok = ok && mbar_wait(bar_v_full(st), (j / NST) & 1, p.status);
+                const uint32_t sV = sV0 + st * Sh::KV_BYTES;
                 for (int i = tid - 64; i < (kBN - valid) * Sh::HALVES * 8; i += 128) {
                     const int rr = valid + i / (Sh::HALVES * 8), rest = i % (Sh::HALVES * 8);
                     sts128(sV + (rest / 8) * (kBN * 128) + rr * 128 + (rest % 8) * 16, 0u, 0u, 0u, 0u);
                 }
+                fence_async_smem();
             }
-            fence_async_smem();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_p_full(sb));
