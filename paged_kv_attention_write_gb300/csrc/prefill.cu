@@ -9,23 +9,37 @@
 // under a token budget, 512 tokens per chunk); TensorSharp "Mistral 3" page,
 // section 11 (paged K/V gather, then fused attention).
 //
-// Grid (query tile, kv head, sequence).  A query tile is 128 rows of
+// A work unit is one query tile of one sequence; a tile is 128 rows of
 // (token, head) pairs of ONE kv head's G query heads (128/G tokens), so each
-// gathered K/V tile serves G heads.  Per 128-key tile j:
-//   S_j = Q K_j^T   tcgen05.mma M128 N128 K=D, fp32 in TMEM (two buffers)
+// gathered K/V tile serves G heads.  An item is a unit for one kv head.
+// Persistent grid: one CTA per SM walks its items back to back, so the fixed
+// cost of a CTA (barrier setup, TMEM allocation, pipeline fill, epilogue) is
+// paid once per SM and the next item's loads and S products overlap the
+// previous item's last P.V and epilogue.  Units differ in cost by their number
+// of key tiles (a tile deep in a long prefix sees many more keys than the first
+// tile of a fresh prompt), so every CTA first ranks all units longest-first
+// from the query and context lengths (a stable counting sort in shared memory,
+// identical in every CTA) and the CTAs deal the ranked items out round by
+// round, alternating direction.
+// Per 128-key tile j:
+//   S_j = Q K_j^T   tcgen05.mma M128 N128 K=D, fp32 in TMEM (three buffers, so
+//                   the S products run up to three tiles ahead)
 //   P_j             one thread per row reads its S row from TMEM: mask,
 //                   online softmax in the log2 domain with lazy rescaling
 //                   (the reference max moves only when a score exceeds it by
 //                   2^8), P_j rounded to bf16/fp16 and written back to TMEM
+//                   over the S row
 //   O  += P_j V_j   tcgen05.mma M128 N=D K128 with A = P from TMEM, fp32 in
 //                   TMEM; V is the MN-major shared-memory operand
-// Warp roles: warps 0 and 6 issue the TMA loads (the Q tile once; per key tile
-// one 3-D box per block through the block table, issued by the lanes in
-// parallel, into separate 3-stage K and V rings: a K stage frees when its S
-// finishes, a V stage when its P.V does), warp 1 issues the MMAs, warps 2-5
-// run the softmax and the epilogue.  All
+// Warp roles: warps 0 and 6 issue the TMA loads (the Q tile; per key tile one
+// 3-D box per block through the block table, issued by the lanes in parallel,
+// into separate K and V rings: a K stage frees when its S finishes, a V stage
+// when its P.V does), warp 1 issues the S products and warp 7 the P.V products
+// (a thread waits for each MMA to be accepted, so one issuer cannot keep the
+// tensor core busy), warps 2-5 run the softmax and the epilogue.  All
 // shared-memory operands use the 128-byte swizzle.  Every wait is an mbarrier
 // wait bounded in time.
+#include <algorithm>
 #include <type_traits>
 
 #include "tma.cuh"
@@ -33,7 +47,7 @@
 namespace pa {
 namespace {
 
-constexpr int kPfThreads = 7 * 32;
+constexpr int kPfThreads = 8 * 32;
 constexpr int kBM = 128;  // query rows per CTA
 constexpr int kBN = 128;  // keys per tile
 constexpr float kRescaleLog2 = 8.f;
@@ -159,9 +173,145 @@ struct PrefillParams {
     const int32_t *block_tables;
     const int32_t *context_lens;
     int max_blocks_per_seq, num_heads, num_kv_heads, block_size, num_blocks, max_context_len;
-    int num_tokens;
+    int num_tokens, num_seqs;
+    int q_tiles;    // query tiles per sequence (of the longest chunk)
+    int num_items;  // num_seqs * q_tiles * num_kv_heads
     float qk_scale_log2;
     int32_t *status;
+};
+
+// ---------------------------------------------------------------- work items and their order
+// A unit is (sequence s, query tile qt), numbered s * q_tiles + qt; an item is (unit, kv
+// head).  Items are ranked unit-major: the units of rank r give items r*Hkv .. r*Hkv+Hkv-1.
+// CTA c of P takes one item per round k, item k*P + c in even rounds and k*P + P-1-c in odd
+// ones, so that each CTA's total of light and heavy items evens out.
+constexpr int kPlanMaxUnits = 4096;  // more units: rank r is unit r (latest tile first)
+constexpr int kPlanBins = 1024;      // key-tile counts; longer units share the last bin
+constexpr int kMaxRounds = 32;       // more items per CTA: no ranking either
+
+__device__ __forceinline__ int64_t round_item(int k, int P, int c) {
+    return (int64_t)k * P + ((k & 1) ? P - 1 - c : c);
+}
+
+// Key tiles the unit (s, qt) runs through; 0 for an empty or invalid unit.
+__device__ __forceinline__ int unit_tiles(const PrefillParams &p, int s, int qt, int TT) {
+    const int q0 = p.query_start_loc[s];
+    const int Lq = p.query_start_loc[s + 1] - q0;
+    if (q0 < 0 || Lq < 0 || (int64_t)q0 + Lq > p.num_tokens || qt * TT >= Lq) return 0;
+    const int C = min(p.context_lens[s], min(p.max_blocks_per_seq * p.block_size, p.max_context_len));
+    if (Lq > C) return 0;
+    return (C - Lq + min(Lq, (qt + 1) * TT) + kBN - 1) / kBN;
+}
+
+// Ranks the units by key tiles, most first, ties in unit order (a stable counting sort in
+// shared memory: every CTA computes the same order), and lists the unit of each of this
+// CTA's rounds in my_units.  Called by every thread; `scratch` is shared memory that
+// nothing else touches until the call returns.
+__device__ void plan_units(const PrefillParams &p, int TT, int P, int c, unsigned char *scratch,
+                           uint16_t *my_units) {
+    const int Q = p.q_tiles, U = p.num_seqs * Q;
+    const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+    constexpr int NT = kPfThreads;
+    auto hslot = [](int b) { return b + (b >> 5); };  // padded: a lane's 32 bins hit 32 banks
+    int *hist = reinterpret_cast<int *>(scratch);
+    uint16_t *wt = reinterpret_cast<uint16_t *>(hist + kPlanBins + kPlanBins / 32);
+    uint16_t *order = wt + kPlanMaxUnits;
+    for (int i = tid; i < kPlanBins + kPlanBins / 32; i += NT) hist[i] = 0;
+    __syncthreads();
+    for (int u = tid; u < U; u += NT) {
+        const int w = min(unit_tiles(p, u / Q, u % Q, TT), kPlanBins - 1);
+        wt[u] = (uint16_t)w;
+        atomicAdd(&hist[hslot(w)], 1);
+    }
+    __syncthreads();
+    if (warp == 0) {
+        // hist[b] <- number of units with more key tiles than b; lane l owns the bins
+        // 1023-32l down to 992-32l
+        int sum = 0;
+        for (int i = 0; i < 32; ++i) sum += hist[hslot(kPlanBins - 1 - (lane * 32 + i))];
+        int inc = sum;
+        for (int o = 1; o < 32; o <<= 1) {
+            const int t = __shfl_up_sync(kFullMask, inc, o);
+            if (lane >= o) inc += t;
+        }
+        int acc = inc - sum;
+        for (int i = 0; i < 32; ++i) {
+            const int b = hslot(kPlanBins - 1 - (lane * 32 + i)), h = hist[b];
+            hist[b] = acc;
+            acc += h;
+        }
+        __syncwarp();
+        // scatter 32 units at a time in unit order; lanes of equal weight take consecutive
+        // ranks and the lowest of them advances the bin's next rank
+        for (int base = 0; base < U; base += 32) {
+            const int u = base + lane;
+            const int w = u < U ? wt[u] : -1;
+            const unsigned peers = __match_any_sync(kFullMask, w);
+            if (u < U) order[hist[hslot(w)] + __popc(peers & ((1u << lane) - 1u))] = (uint16_t)u;
+            __syncwarp();
+            if (u < U && lane == __ffs(peers) - 1) hist[hslot(w)] += __popc(peers);
+            __syncwarp();
+        }
+    }
+    __syncthreads();
+    for (int k = tid; k < kMaxRounds; k += NT) {
+        const int64_t idx = round_item(k, P, c);
+        if (idx < p.num_items) my_units[k] = order[idx / p.num_kv_heads];
+    }
+    __syncthreads();
+    // the scratch becomes a TMA destination: order these generic accesses before it
+    fence_async_smem();
+}
+
+// One item's scalars.  fetch() issues the loads of round k; resolve() turns them into the
+// item (false when it has no rows, with a status bit when the inputs are invalid).
+struct PfItem {
+    int s, qt, g, q0, Lq, C, tok_begin, pos0, kv_end, n_tiles;
+};
+struct PfCursor {
+    bool have;
+    int unit, g, q0, q1, C;
+
+    __device__ __forceinline__ void fetch(const PrefillParams &p, int k, bool planned,
+                                          const uint16_t *my_units) {
+        const int P = gridDim.x, c = blockIdx.x;
+        const int64_t idx = round_item(k, P, c);
+        have = idx < p.num_items;
+        if (!have) return;
+        const int rank = (int)(idx / p.num_kv_heads), Q = p.q_tiles;
+        g = (int)(idx % p.num_kv_heads);
+        unit = planned ? my_units[k] : (rank / Q) * Q + Q - 1 - rank % Q;
+        const int s = unit / Q;
+        q0 = p.query_start_loc[s];
+        q1 = p.query_start_loc[s + 1];
+        C = p.context_lens[s];
+    }
+
+    __device__ __forceinline__ bool resolve(const PrefillParams &p, int TT, bool rep, PfItem &it) const {
+        it.s = unit / p.q_tiles;
+        it.qt = unit % p.q_tiles;
+        it.g = g;
+        it.q0 = q0;
+        it.Lq = q1 - q0;
+        if (q0 < 0 || it.Lq < 0 || (int64_t)q0 + it.Lq > p.num_tokens) {  // never index past the query
+            if (rep) report(p.status, PA_DEVERR_QUERY);
+            return false;
+        }
+        if (it.qt * TT >= it.Lq) return false;
+        const int cap = min(p.max_blocks_per_seq * p.block_size, p.max_context_len);
+        int Cc = C;
+        if (Cc > cap || it.Lq > Cc) {
+            if (rep) report(p.status, Cc > cap ? PA_DEVERR_CONTEXT : PA_DEVERR_QUERY);
+            if (Cc > cap) Cc = cap;
+            if (it.Lq > Cc) return false;
+        }
+        it.C = Cc;
+        it.tok_begin = it.qt * TT;
+        it.pos0 = Cc - it.Lq;                                     // absolute position of chunk row 0
+        it.kv_end = it.pos0 + min(it.Lq, it.tok_begin + TT);      // keys visible to the tile's last row
+        it.n_tiles = (it.kv_end + kBN - 1) / kBN;
+        return true;
+    }
 };
 
 template <int D>
@@ -169,73 +319,71 @@ struct PfShape {
     static constexpr int HALVES = D / 64;             // 128-byte swizzle atoms along D
     static constexpr int Q_BYTES = kBM * D * 2;       // [half][128 rows][128 B]
     static constexpr int KV_BYTES = kBN * D * 2;      // one K (or V) stage, same layout
-    static constexpr int NST = 3;                     // K stages and V stages
+    static constexpr int NQ = D == 64 ? 2 : 1;        // Q buffers
+    static constexpr int NK = D == 64 ? 4 : 3;        // K stages
+    static constexpr int NV = D == 64 ? 4 : 3;        // V stages
     static constexpr int OFF_Q = 0;
-    static constexpr int OFF_K = OFF_Q + Q_BYTES;
-    static constexpr int OFF_V = OFF_K + NST * KV_BYTES;
-    static constexpr int OFF_BAR = OFF_V + NST * KV_BYTES;
-    static constexpr int SMEM = 1024 + OFF_BAR + 256;
+    static constexpr int OFF_K = OFF_Q + NQ * Q_BYTES;
+    static constexpr int OFF_V = OFF_K + NK * KV_BYTES;
+    static constexpr int OFF_BAR = OFF_V + NV * KV_BYTES;
+    static constexpr int SMEM = 1024 + OFF_BAR + 512;
     static_assert(SMEM <= 227 * 1024, "shared memory budget");
+    // the unit plan borrows the K ring before the first load
+    static_assert((kPlanBins + kPlanBins / 32) * 4 + 2 * kPlanMaxUnits * 2 <= NK * KV_BYTES,
+                  "plan scratch fits the K ring");
 };
 
-// TMEM columns: S (fp32, 128 keys) in two buffers, O (fp32, D), P (two bf16/fp16 keys
-// per column, 128 keys) in two buffers.
+// TMEM columns: S (fp32, 128 keys) in three buffers, S_t in buffer t % 3; P_t (two
+// bf16/fp16 keys per column) is written over the first 64 columns of S_t's buffer once
+// S_t has been read; O (fp32, D) after them.  Three buffers let the S products run up to
+// three tiles ahead of the P.V products, so the softmax never waits for an S.
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemS0 = 0, kTmemO = 256, kTmemP0 = 384;
+constexpr int kSBufs = 3;
+constexpr uint32_t kTmemO = kSBufs * kBN;
 
 template <class T, int D, int G>
 __global__ void __launch_bounds__(kPfThreads, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                   const __grid_constant__ CUtensorMap vmap, const PrefillParams p) {
     using Sh = PfShape<D>;
-    constexpr int NST = Sh::NST;
+    constexpr int NQ = Sh::NQ, NK = Sh::NK, NV = Sh::NV;
     constexpr int TT = kBM / G;  // query tokens per tile
     constexpr int KSTEPS_S = D / 16, KSTEPS_PV = kBN / 16;
     constexpr bool kBf16 = std::is_same<T, BF16>::value;
     constexpr uint32_t IDESC_S = mma_idesc(128, kBN, kBf16, false);
     constexpr uint32_t IDESC_PV = mma_idesc(128, D, kBf16, true);
+    static_assert(kTmemO + D <= kTmemCols, "TMEM budget");
 
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
-    const uint32_t sQ = sbase + Sh::OFF_Q, sK0 = sbase + Sh::OFF_K, sV0 = sbase + Sh::OFF_V;
+    const uint32_t sQ0 = sbase + Sh::OFF_Q, sK0 = sbase + Sh::OFF_K, sV0 = sbase + Sh::OFF_V;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Sh::OFF_BAR);
     const uint32_t b0 = smem_u32(bars);
-    const uint32_t bar_q = b0;
-    auto bar_k_full = [&](int i) { return b0 + 8 * (1 + i); };            // K stage landed
-    auto bar_k_empty = [&](int i) { return b0 + 8 * (1 + NST + i); };     // S of that K finished
-    auto bar_v_full = [&](int i) { return b0 + 8 * (1 + 2 * NST + i); };  // V stage landed
-    auto bar_v_empty = [&](int i) { return b0 + 8 * (1 + 3 * NST + i); }; // P.V of that V finished
-    constexpr int B2 = 1 + 4 * NST;
-    auto bar_s_full = [&](int i) { return b0 + 8 * (B2 + i); };      // S buffer written
-    auto bar_s_free = [&](int i) { return b0 + 8 * (B2 + 2 + i); };  // S buffer read by the softmax
-    auto bar_p_full = [&](int i) { return b0 + 8 * (B2 + 4 + i); };  // P buffer written
-    auto bar_pv_done = [&](int i) { return b0 + 8 * (B2 + 6 + i); }; // P.V of that P finished
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + B2 + 8);
-    int *abort_flag = reinterpret_cast<int *>(bars + B2 + 9);
+    auto bar = [&](int i) { return b0 + 8 * i; };
+    constexpr int BQF = 0;              // Q buffer landed
+    constexpr int BQE = BQF + NQ;       // last S of that Q's item finished
+    constexpr int BKF = BQE + NQ;       // K stage landed
+    constexpr int BKE = BKF + NK;       // S of that K finished
+    constexpr int BVF = BKE + NK;       // V stage landed
+    constexpr int BVE = BVF + NV;       // P.V of that V finished
+    constexpr int BSF = BVE + NV;       // S buffer written
+    constexpr int BPF = BSF + kSBufs;   // P written over that S buffer
+    constexpr int BPV = BPF + kSBufs;   // P.V of that buffer's P finished
+    constexpr int NBAR = BPV + kSBufs;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + NBAR);
+    int *abort_flag = reinterpret_cast<int *>(bars + NBAR) + 1;
+    uint16_t *my_units = reinterpret_cast<uint16_t *>(bars + NBAR + 1);
+    static_assert((NBAR + 1) * 8 + kMaxRounds * 2 <= 512, "barrier area");
 
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
-    const int g = blockIdx.y, s = blockIdx.z;
-    const int qt = gridDim.x - 1 - blockIdx.x;  // heaviest (latest) tiles first
     const int Hq = p.num_heads, bs = p.block_size;
 
     // ---- prologue independent of earlier kernels
     if (tid == 0) {
         *abort_flag = 0;
-        mbar_init(bar_q, 1);
-        for (int i = 0; i < NST; ++i) {
-            mbar_init(bar_k_full(i), 1);
-            mbar_init(bar_k_empty(i), 1);
-            mbar_init(bar_v_full(i), 1);
-            mbar_init(bar_v_empty(i), 1);
-        }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(bar_s_full(i), 1);
-            mbar_init(bar_s_free(i), 4);
-            mbar_init(bar_p_full(i), 4);
-            mbar_init(bar_pv_done(i), 1);
-        }
+        for (int i = 0; i < NBAR; ++i) mbar_init(bar(i), (i >= BPF && i < BPF + kSBufs) ? 4 : 1);
         fence_barrier_init();
         prefetch_tensormap(&qmap);
         prefetch_tensormap(&kmap);
@@ -244,26 +392,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
     pdl_wait_previous();
     pdl_launch_dependents();
 
-    const int q0 = p.query_start_loc[s];
-    const int Lq = p.query_start_loc[s + 1] - q0;
-    int C = p.context_lens[s];
-    if (q0 < 0 || Lq < 0 || (int64_t)q0 + Lq > p.num_tokens) {  // never index past the query
-        if (tid == 0 && blockIdx.x == 0 && g == 0) report(p.status, PA_DEVERR_QUERY);
-        return;
-    }
-    if (qt * TT >= Lq) return;
-    const int cap = min(p.max_blocks_per_seq * bs, p.max_context_len);
-    if (C > cap || Lq > C) {
-        if (tid == 0 && qt * TT == 0 && g == 0) report(p.status, C > cap ? PA_DEVERR_CONTEXT : PA_DEVERR_QUERY);
-        if (C > cap) C = cap;
-        if (Lq > C) return;
-    }
-    const int tok_begin = qt * TT;
-    const int tok_end = min(Lq, tok_begin + TT);
-    const int pos0 = C - Lq;                 // absolute position of chunk row 0
-    const int kv_end = pos0 + tok_end;       // keys visible to the tile's last row
-    const int n_tiles = (kv_end + kBN - 1) / kBN;
-    const int32_t *bt = p.block_tables + (int64_t)s * p.max_blocks_per_seq;
+    const int rounds = (p.num_items + gridDim.x - 1) / gridDim.x;
+    const bool planned = p.num_seqs * p.q_tiles <= kPlanMaxUnits && rounds <= kMaxRounds;
+    if (planned) plan_units(p, TT, gridDim.x, blockIdx.x, smem + Sh::OFF_K, my_units);
 
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -276,97 +407,154 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     volatile int *abort_v = abort_flag;
+    // Every role walks the same items (a cursor runs one round ahead so that the next
+    // item's scalars are in flight) and counts the same global key tiles t, which pick
+    // ring stages, S/P buffers and their phases; vi counts the items with rows and picks
+    // the Q buffer.
+    PfCursor cur;
 
     if (warp == 0 || warp == 6) {
-        // ============================================ producers (TMA): warp 0 loads K, warp 6 V
-        // A K stage frees when its S finishes, a V stage when its P.V does; each warp
-        // runs ahead on its own ring.  Lane b fetches the block id of the tile's b-th
-        // block two tiles ahead and issues that block's boxes; lane 0 posts the
-        // tile's transaction bytes first and arrives after the warp has issued.
+        // ============================================ producers (TMA): warp 0 loads Q and K, warp 6 V
+        // A K stage frees when its S finishes, a V stage when its P.V does, the Q buffer
+        // when its item's last S does.  Lane b fetches the block id of the tile's b-th
+        // block two tiles ahead and issues that block's boxes; lane 0 posts the tile's
+        // transaction bytes first and arrives after the warp has issued.
         const bool is_k = warp == 0;
         const CUtensorMap *map = is_k ? &kmap : &vmap;
         const uint32_t ring = is_k ? sK0 : sV0;
+        const int NS = is_k ? NK : NV;
+        const int bar_full = is_k ? BKF : BVF, bar_empty = is_k ? BKE : BVE;
         const uint64_t policy = policy_evict_first();
         const int nb = kBN / bs;  // blocks per key tile (4, 8 or 16)
         const uint32_t box_bytes = (uint32_t)bs * 128;  // one block of one kv head, one D half
-        auto block_id = [&](int j) {
-            const int key = j * kBN + lane * bs;
-            return (lane < nb && j < n_tiles && key < kv_end) ? bt[key / bs] : -1;
-        };
-        if (is_k && lane == 0) {  // Q: tokens [tok_begin, +TT) x heads [g*G, +G), one D half per box
-            mbar_expect_tx(bar_q, Sh::Q_BYTES);
-            for (int hf = 0; hf < Sh::HALVES; ++hf)
-                tma_load_3d(sQ + hf * (kBM * 128), &qmap, hf * 64, g * G, q0 + tok_begin, bar_q, policy);
-            mbar_arrive(bar_q);
-        }
-        int id0 = block_id(0), id1 = block_id(1);
-        for (int j = 0; j < n_tiles; ++j) {
-            const int my_id = id0;
-            id0 = id1;
-            id1 = block_id(j + 2);
-            const int st = j % NST;
-            const uint32_t empty = is_k ? bar_k_empty(st) : bar_v_empty(st);
-            const uint32_t full = is_k ? bar_k_full(st) : bar_v_full(st);
-            int ok = 1;
-            if (lane == 0) ok = !*abort_v && mbar_wait(empty, ((j / NST) & 1) ^ 1, p.status);
-            if (!__shfl_sync(kFullMask, ok, 0)) {
-                if (lane == 0) *abort_v = 1;
-                break;
-            }
-            const bool in_range = lane < nb && j * kBN + lane * bs < kv_end;
-            const bool valid = in_range && my_id >= 0 && my_id < p.num_blocks;
-            if (in_range && !valid) report(p.status, PA_DEVERR_BLOCK_ID);  // never dereferenced
-            const unsigned mine = __ballot_sync(kFullMask, valid);
-            if (lane == 0) mbar_expect_tx(full, __popc(mine) * Sh::HALVES * box_bytes);
-            __syncwarp();
-            if (valid) {
-                const uint32_t dst = ring + st * Sh::KV_BYTES + lane * box_bytes;
-                for (int hf = 0; hf < Sh::HALVES; ++hf)
-                    tma_load_3d(dst + hf * (kBN * 128), map, hf * 64, g, my_id * bs, full, policy);
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(full);
-        }
-    } else if (warp == 1) {
-        // ============================================ MMA issuer
-        if (lane == 0) {
-            bool ok = mbar_wait(bar_q, 0, p.status);
-            auto pv = [&](int t) {  // O += P_t V_t, P from TMEM
-                const int pb = t & 1, st = t % NST;
-                if (!ok || !mbar_wait(bar_v_full(st), (t / NST) & 1, p.status) ||
-                    !mbar_wait(bar_p_full(pb), (t >> 1) & 1, p.status)) {
-                    ok = false;
-                    return;
-                }
-                tc_fence_after();
-                const uint32_t sV = sV0 + st * Sh::KV_BYTES;
-#pragma unroll
-                for (int kk = 0; kk < KSTEPS_PV; ++kk) {
-                    const uint64_t db = smem_desc(sV + kk * 16 * 128, kBN * 128, 1024);
-                    mma_f16_tmem_a(tmem + kTmemO, tmem + kTmemP0 + pb * (kBN / 2) + kk * 8, db, IDESC_PV,
-                                   (t > 0 || kk > 0) ? 1u : 0u);
-                }
-                mma_commit(bar_pv_done(pb));
-                mma_commit(bar_v_empty(st));
+        bool ok = true;
+        int t = 0, vi = 0;
+        cur.fetch(p, 0, planned, my_units);
+        for (int k = 0; ok && cur.have; ++k) {
+            PfItem it;
+            const bool live = cur.resolve(p, TT, false, it);
+            cur.fetch(p, k + 1, planned, my_units);
+            if (!live) continue;
+            const int32_t *bt = p.block_tables + (int64_t)it.s * p.max_blocks_per_seq;
+            auto block_id = [&](int j) {
+                const int key = j * kBN + lane * bs;
+                return (lane < nb && j < it.n_tiles && key < it.kv_end) ? bt[key / bs] : -1;
             };
-            for (int j = 0; j < n_tiles && ok; ++j) {
-                const int st = j % NST, sb = j & 1;
-                ok = !*abort_v && mbar_wait(bar_k_full(st), (j / NST) & 1, p.status);
-                if (ok && j >= 2) ok = mbar_wait(bar_s_free(sb), ((j - 2) >> 1) & 1, p.status);
-                if (!ok) break;
-                tc_fence_after();
-                const uint32_t sK = sK0 + st * Sh::KV_BYTES;
-#pragma unroll
-                for (int ks = 0; ks < KSTEPS_S; ++ks) {
-                    const uint32_t off = (ks / 4) * (kBM * 128) + (ks % 4) * 32;
-                    mma_f16(tmem + kTmemS0 + sb * kBN, smem_desc(sQ + off, 16, 1024),
-                            smem_desc(sK + off, 16, 1024), IDESC_S, ks > 0 ? 1u : 0u);
+            int id0 = block_id(0), id1 = block_id(1);
+            if (is_k) {  // Q: tokens [tok_begin, +TT) x heads [g*G, +G), one D half per box
+                const int qb = vi % NQ;
+                int q_ok = 1;
+                if (lane == 0) {
+                    q_ok = !*abort_v && mbar_wait(bar(BQE + qb), ((vi / NQ) & 1) ^ 1, p.status);
+                    if (q_ok) {
+                        mbar_expect_tx(bar(BQF + qb), Sh::Q_BYTES);
+                        for (int hf = 0; hf < Sh::HALVES; ++hf)
+                            tma_load_3d(sQ0 + qb * Sh::Q_BYTES + hf * (kBM * 128), &qmap, hf * 64,
+                                        it.g * G, it.q0 + it.tok_begin, bar(BQF + qb), policy);
+                        mbar_arrive(bar(BQF + qb));
+                    }
                 }
-                mma_commit(bar_s_full(sb));
-                mma_commit(bar_k_empty(st));
-                if (j >= 1) pv(j - 1);
+                if (!__shfl_sync(kFullMask, q_ok, 0)) {
+                    ok = false;
+                    break;
+                }
             }
-            if (ok) pv(n_tiles - 1);
+            for (int j = 0; j < it.n_tiles; ++j, ++t) {
+                const int my_id = id0;
+                id0 = id1;
+                id1 = block_id(j + 2);
+                const int st = t % NS;
+                const uint32_t full = bar(bar_full + st);
+                int w_ok = 1;
+                if (lane == 0) w_ok = !*abort_v && mbar_wait(bar(bar_empty + st), ((t / NS) & 1) ^ 1, p.status);
+                if (!__shfl_sync(kFullMask, w_ok, 0)) {
+                    ok = false;
+                    break;
+                }
+                const bool in_range = lane < nb && j * kBN + lane * bs < it.kv_end;
+                const bool valid = in_range && my_id >= 0 && my_id < p.num_blocks;
+                if (in_range && !valid) report(p.status, PA_DEVERR_BLOCK_ID);  // never dereferenced
+                const unsigned mine = __ballot_sync(kFullMask, valid);
+                if (lane == 0) mbar_expect_tx(full, __popc(mine) * Sh::HALVES * box_bytes);
+                __syncwarp();
+                if (valid) {
+                    const uint32_t dst = ring + st * Sh::KV_BYTES + lane * box_bytes;
+                    for (int hf = 0; hf < Sh::HALVES; ++hf)
+                        tma_load_3d(dst + hf * (kBN * 128), map, hf * 64, it.g, my_id * bs, full, policy);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(full);
+            }
+            ++vi;
+        }
+        if (!ok && lane == 0) *abort_v = 1;
+    } else if (warp == 1) {
+        // ============================================ S issuer: S_t = Q K_t^T
+        // The S and P.V products are issued by two threads (warps 1 and 7): one thread
+        // waits for each tcgen05.mma to be accepted, so a single issuer keeps the tensor
+        // core only about half busy.  S runs up to three tiles ahead of the P.V products;
+        // S_t overwrites the P of tile t-3, so it waits until that P.V has finished.
+        if (lane == 0) {
+            bool ok = true;
+            int t = 0, vi = 0;
+            cur.fetch(p, 0, planned, my_units);
+            for (int k = 0; ok && cur.have; ++k) {
+                PfItem it;
+                const bool live = cur.resolve(p, TT, false, it);
+                cur.fetch(p, k + 1, planned, my_units);
+                if (!live) continue;
+                const int qb = vi % NQ;
+                ok = !*abort_v && mbar_wait(bar(BQF + qb), (vi / NQ) & 1, p.status);
+                const uint32_t sQ = sQ0 + qb * Sh::Q_BYTES;
+                for (int j = 0; j < it.n_tiles && ok; ++j, ++t) {
+                    const int st = t % NK, sb = t % kSBufs;
+                    if (t >= kSBufs) ok = mbar_wait(bar(BPV + sb), (t / kSBufs - 1) & 1, p.status);
+                    ok = ok && !*abort_v && mbar_wait(bar(BKF + st), (t / NK) & 1, p.status);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint32_t sK = sK0 + st * Sh::KV_BYTES;
+#pragma unroll
+                    for (int ks = 0; ks < KSTEPS_S; ++ks) {
+                        const uint32_t off = (ks / 4) * (kBM * 128) + (ks % 4) * 32;
+                        mma_f16(tmem + sb * kBN, smem_desc(sQ + off, 16, 1024), smem_desc(sK + off, 16, 1024),
+                                IDESC_S, ks > 0 ? 1u : 0u);
+                    }
+                    mma_commit(bar(BSF + sb));
+                    mma_commit(bar(BKE + st));
+                }
+                if (ok) mma_commit(bar(BQE + qb));  // the Q buffer is free once these S finish
+                ++vi;
+            }
+            if (!ok) *abort_v = 1;
+        }
+    } else if (warp == 7) {
+        // ============================================ P.V issuer: O += P_t V_t, P from TMEM
+        if (lane == 0) {
+            bool ok = true;
+            int t = 0;
+            cur.fetch(p, 0, planned, my_units);
+            for (int k = 0; ok && cur.have; ++k) {
+                PfItem it;
+                const bool live = cur.resolve(p, TT, false, it);
+                cur.fetch(p, k + 1, planned, my_units);
+                if (!live) continue;
+                for (int j = 0; j < it.n_tiles && ok; ++j, ++t) {
+                    const int pb = t % kSBufs, st = t % NV;
+                    ok = !*abort_v && mbar_wait(bar(BPF + pb), (t / kSBufs) & 1, p.status) &&
+                         mbar_wait(bar(BVF + st), (t / NV) & 1, p.status);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint32_t sV = sV0 + st * Sh::KV_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < KSTEPS_PV; ++kk) {
+                        const uint64_t db = smem_desc(sV + kk * 16 * 128, kBN * 128, 1024);
+                        mma_f16_tmem_a(tmem + kTmemO, tmem + pb * kBN + kk * 8, db, IDESC_PV,
+                                       (j > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    mma_commit(bar(BPV + pb));
+                    mma_commit(bar(BVE + st));
+                }
+            }
             if (!ok) *abort_v = 1;
         }
     } else {
@@ -374,144 +562,150 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
         const int quarter = warp & 3;            // TMEM lanes this warp may access
         const int row = quarter * 32 + lane;     // query row of the tile
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-        // rows past the chunk (a ragged last tile) are computed but never stored; they
-        // see exactly the keys that were loaded
-        const int pos = min(pos0 + tok_begin + row / G, kv_end - 1);
-        const int row0_pos = pos0 + tok_begin;  // position of the tile's first row
-        float m_ref = -INFINITY, l = 0.f;
+        const uint32_t tO = tmem + lane_off + kTmemO;
         bool ok = true;
-        for (int j = 0; j < n_tiles; ++j) {
-            const int sb = j & 1;
-            ok = ok && !*abort_v && mbar_wait(bar_s_full(sb), (j >> 1) & 1, p.status);
-            if (!ok) {
-                *abort_v = 1;
-                break;
+        int t = 0;
+        cur.fetch(p, 0, planned, my_units);
+        for (int k = 0; ok && cur.have; ++k) {
+            PfItem it;
+            const bool live = cur.resolve(p, TT, warp == 2 && lane == 0, it);
+            cur.fetch(p, k + 1, planned, my_units);
+            if (!live) continue;
+            // rows past the chunk (a ragged last tile) are computed but never stored; they
+            // see exactly the keys that were loaded
+            const int pos = min(it.pos0 + it.tok_begin + row / G, it.kv_end - 1);
+            const int row0_pos = it.pos0 + it.tok_begin;  // position of the tile's first row
+            float m_ref = -INFINITY, l = 0.f;
+            for (int j = 0; j < it.n_tiles; ++j, ++t) {
+                const int sb = t % kSBufs;
+                ok = ok && !*abort_v && mbar_wait(bar(BSF + sb), (t / kSBufs) & 1, p.status);
+                if (!ok) break;
+                tc_fence_after();
+                const int k0 = j * kBN;
+                const uint32_t tS = tmem + lane_off + sb * kBN;
+                float sv[kBN];
+                {
+                    uint32_t r0[32], r1[32], r2[32], r3[32];
+                    tmem_ld32(tS, r0);
+                    tmem_ld32(tS + 32, r1);
+                    tmem_ld32(tS + 64, r2);
+                    tmem_ld32(tS + 96, r3);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        sv[i] = __uint_as_float(r0[i]);
+                        sv[32 + i] = __uint_as_float(r1[i]);
+                        sv[64 + i] = __uint_as_float(r2[i]);
+                        sv[96 + i] = __uint_as_float(r3[i]);
+                    }
+                }
+                // mask (keys k0 .. k0+lim-1 are visible; only the last tiles need it) and row
+                // max of the raw scores, in eight independent chains
+                const int lim = min(pos + 1, it.C) - k0;
+                if (k0 + kBN > row0_pos + 1 || k0 + kBN > it.C) {  // tile-uniform
+#pragma unroll
+                    for (int c = 0; c < kBN; ++c) sv[c] = c < lim ? sv[c] : -INFINITY;
+                }
+                float mx8[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) mx8[i] = sv[i];
+#pragma unroll
+                for (int c = 8; c < kBN; ++c) mx8[c % 8] = fmaxf(mx8[c % 8], sv[c]);
+                const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                       fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) *
+                                 p.qk_scale_log2;
+                // lazy rescale; warp-uniform because the O row is read and written by the
+                // whole warp (tcgen05.ld / st)
+                const bool grow = mx > m_ref + kRescaleLog2;
+                if (__any_sync(kFullMask, grow)) {
+                    const float m_new = grow ? mx : m_ref;
+                    const float alpha = m_new == m_ref ? 1.f : fast_exp2(m_ref - m_new);  // 0 from -inf
+                    l *= alpha;
+                    m_ref = m_new;
+                    if (j >= 1) {  // O holds tiles < j: wait for the last P.V, then scale the row
+                        ok = ok && mbar_wait(bar(BPV + (t - 1) % kSBufs), ((t - 1) / kSBufs) & 1, p.status);
+                        tc_fence_after();
+#pragma unroll
+                        for (int c0 = 0; c0 < D; c0 += 32) {
+                            uint32_t r[32];
+                            tmem_ld32(tO + c0, r);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+                            tmem_st32(tO + c0, r);
+                        }
+                        tmem_wait_st();
+                    }
+                }
+                // P row over the S row just read: 128 keys packed two per TMEM column (the
+                // P.V of this buffer's previous tile finished before this S was issued)
+                const float sc = p.qk_scale_log2, neg_m = -m_ref;
+                float rs4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t w[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const int c = half * 64 + 2 * i;
+                        w[i] = pack2<T>(fast_exp2(fmaf(sv[c], sc, neg_m)), fast_exp2(fmaf(sv[c + 1], sc, neg_m)));
+                        rs4[i & 3] += unpack_sum<T>(w[i]);
+                    }
+                    tmem_st32(tS + half * 32, w);
+                }
+                tmem_wait_st();
+                l += (rs4[0] + rs4[1]) + (rs4[2] + rs4[3]);
+                // keys past kv_end in this tile (not loaded, or past the context): zero V rows,
+                // so that 0-weight rows never meet stale or NaN data
+                if (k0 + kBN > it.kv_end) {
+                    const int valid = it.kv_end - k0, st = t % NV;
+                    ok = ok && mbar_wait(bar(BVF + st), (t / NV) & 1, p.status);
+                    const uint32_t sV = sV0 + st * Sh::KV_BYTES;
+                    for (int i = tid - 64; i < (kBN - valid) * Sh::HALVES * 8; i += 128) {
+                        const int rr = valid + i / (Sh::HALVES * 8), rest = i % (Sh::HALVES * 8);
+                        sts128(sV + (rest / 8) * (kBN * 128) + rr * 128 + (rest % 8) * 16, 0u, 0u, 0u, 0u);
+                    }
+                    fence_async_smem();
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(BPF + sb));
             }
+            if (!ok) break;
+            // ---- epilogue: O / l for the rows of this chunk.  The next item's first P.V
+            // (which overwrites O) waits for P written later by these same threads.
+            const int last = t - 1;
+            ok = mbar_wait(bar(BPV + last % kSBufs), (last / kSBufs) & 1, p.status);
             tc_fence_after();
-            const int k0 = j * kBN;
-            float sv[kBN];
-            {
-                uint32_t r0[32], r1[32], r2[32], r3[32];
-                const uint32_t sa = tmem + lane_off + kTmemS0 + sb * kBN;
-                tmem_ld32(sa, r0);
-                tmem_ld32(sa + 32, r1);
-                tmem_ld32(sa + 64, r2);
-                tmem_ld32(sa + 96, r3);
+            const int tok = it.tok_begin + row / G;
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            const int64_t orow = ((int64_t)(it.q0 + tok) * Hq + it.g * G + row % G) * D;
+#pragma unroll
+            for (int c0 = 0; c0 < D; c0 += 32) {
+                uint32_t r[32];
+                tmem_ld32(tO + c0, r);
                 tmem_wait_ld();
+                if (ok && tok < it.Lq) {
+                    if (p.out_dtype == PA_F32) {
+                        float4 *o = reinterpret_cast<float4 *>(static_cast<float *>(p.out) + orow + c0);
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    sv[i] = __uint_as_float(r0[i]);
-                    sv[32 + i] = __uint_as_float(r1[i]);
-                    sv[64 + i] = __uint_as_float(r2[i]);
-                    sv[96 + i] = __uint_as_float(r3[i]);
-                }
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar_s_free(sb));  // the S buffer may be overwritten
-            // mask (keys k0 .. k0+lim-1 are visible; only the last tiles need it) and row
-            // max of the raw scores, in eight independent chains
-            const int lim = min(pos + 1, C) - k0;
-            if (k0 + kBN > row0_pos + 1 || k0 + kBN > C) {  // tile-uniform
+                        for (int i = 0; i < 8; ++i)
+                            o[i] = make_float4(__uint_as_float(r[4 * i]) * inv, __uint_as_float(r[4 * i + 1]) * inv,
+                                               __uint_as_float(r[4 * i + 2]) * inv, __uint_as_float(r[4 * i + 3]) * inv);
+                    } else {
 #pragma unroll
-                for (int c = 0; c < kBN; ++c) sv[c] = c < lim ? sv[c] : -INFINITY;
-            }
-            float mx8[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) mx8[i] = sv[i];
-#pragma unroll
-            for (int c = 8; c < kBN; ++c) mx8[c % 8] = fmaxf(mx8[c % 8], sv[c]);
-            const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                                   fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) *
-                             p.qk_scale_log2;
-            // lazy rescale; warp-uniform because the O row is read and written by the
-            // whole warp (tcgen05.ld / st)
-            const bool grow = mx > m_ref + kRescaleLog2;
-            if (__any_sync(kFullMask, grow)) {
-                const float m_new = grow ? mx : m_ref;
-                const float alpha = m_new == m_ref ? 1.f : fast_exp2(m_ref - m_new);  // 0 from -inf
-                l *= alpha;
-                m_ref = m_new;
-                if (j >= 1) {  // O holds tiles < j: wait for the last P.V, then scale the row
-                    ok = ok && mbar_wait(bar_pv_done((j - 1) & 1), ((j - 1) >> 1) & 1, p.status);
-                    tc_fence_after();
-#pragma unroll
-                    for (int c0 = 0; c0 < D; c0 += 32) {
-                        uint32_t r[32];
-                        tmem_ld32(tmem + lane_off + kTmemO + c0, r);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-                        tmem_st32(tmem + lane_off + kTmemO + c0, r);
-                    }
-                    tmem_wait_st();
-                }
-            }
-            // the P buffer sb was read by the P.V of tile j-2
-            if (j >= 2) ok = ok && mbar_wait(bar_pv_done(sb), ((j - 2) >> 1) & 1, p.status);
-            // P row: 128 keys packed two per TMEM column
-            const float sc = p.qk_scale_log2, neg_m = -m_ref;
-            float rs4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                uint32_t w[32];
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int c = half * 64 + 2 * i;
-                    w[i] = pack2<T>(fast_exp2(fmaf(sv[c], sc, neg_m)), fast_exp2(fmaf(sv[c + 1], sc, neg_m)));
-                    rs4[i & 3] += unpack_sum<T>(w[i]);
-                }
-                tmem_st32(tmem + lane_off + kTmemP0 + sb * (kBN / 2) + half * 32, w);
-            }
-            tmem_wait_st();
-            l += (rs4[0] + rs4[1]) + (rs4[2] + rs4[3]);
-            // keys past kv_end in this tile (not loaded, or past the context): zero V rows,
-            // so that 0-weight rows never meet stale or NaN data
-            if (k0 + kBN > kv_end) {
-                const int valid = kv_end - k0, st = j % NST;
-                ok = ok && mbar_wait(bar_v_full(st), (j / NST) & 1, p.status);
-                const uint32_t sV = sV0 + st * Sh::KV_BYTES;
-                for (int i = tid - 64; i < (kBN - valid) * Sh::HALVES * 8; i += 128) {
-                    const int rr = valid + i / (Sh::HALVES * 8), rest = i % (Sh::HALVES * 8);
-                    sts128(sV + (rest / 8) * (kBN * 128) + rr * 128 + (rest % 8) * 16, 0u, 0u, 0u, 0u);
-                }
-                fence_async_smem();
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar_p_full(sb));
-        }
-        // ---- epilogue: O / l for the rows of this chunk
-        const int last = n_tiles - 1;
-        if (ok) ok = mbar_wait(bar_pv_done(last & 1), (last >> 1) & 1, p.status);
-        tc_fence_after();
-        const int tok = tok_begin + row / G;
-        const float inv = l > 0.f ? 1.f / l : 0.f;
-        const int64_t orow = ((int64_t)(q0 + tok) * Hq + g * G + row % G) * D;
-#pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 32) {
-            uint32_t r[32];
-            tmem_ld32(tmem + lane_off + kTmemO + c0, r);
-            tmem_wait_ld();
-            if (ok && tok < Lq) {
-                if (p.out_dtype == PA_F32) {
-                    float4 *o = reinterpret_cast<float4 *>(static_cast<float *>(p.out) + orow + c0);
-#pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        o[i] = make_float4(__uint_as_float(r[4 * i]) * inv, __uint_as_float(r[4 * i + 1]) * inv,
-                                           __uint_as_float(r[4 * i + 2]) * inv, __uint_as_float(r[4 * i + 3]) * inv);
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const float a = __uint_as_float(r[2 * i]) * inv, b = __uint_as_float(r[2 * i + 1]) * inv;
-                        if (p.out_dtype == PA_F16)
-                            store_out(static_cast<__half *>(p.out) + orow + c0 + 2 * i, a, b);
-                        else
-                            store_out(static_cast<__nv_bfloat16 *>(p.out) + orow + c0 + 2 * i, a, b);
+                        for (int i = 0; i < 16; ++i) {
+                            const float a = __uint_as_float(r[2 * i]) * inv, b = __uint_as_float(r[2 * i + 1]) * inv;
+                            if (p.out_dtype == PA_F16)
+                                store_out(static_cast<__half *>(p.out) + orow + c0 + 2 * i, a, b);
+                            else
+                                store_out(static_cast<__nv_bfloat16 *>(p.out) + orow + c0 + 2 * i, a, b);
+                        }
                     }
                 }
             }
+            tc_fence_before();
         }
+        if (!ok) *abort_v = 1;
     }
     // ---- teardown: every TMEM access has completed before the columns are released
     tc_fence_before();
@@ -536,8 +730,15 @@ int launch_typed(const PrefillParams &prm, const CUtensorMap &qm, const CUtensor
             return PA_ERR_CUDA;
         configured_device = dev;
     }
-    dim3 grid((max_query_len + TT - 1) / TT, prm.num_kv_heads, num_seqs);
-    return launch_pdl(prefill_tc_kernel<T, D, G>, grid, dim3(kPfThreads), smem, st, qm, km, vm, prm) ==
+    PrefillParams p = prm;
+    p.q_tiles = (max_query_len + TT - 1) / TT;
+    const int64_t items = (int64_t)p.q_tiles * num_seqs * prm.num_kv_heads;
+    if (items > INT32_MAX) return PA_ERR_INVALID_ARG;
+    p.num_items = (int)items;
+    // one persistent CTA per SM (the shared memory allows one)
+    const int sms = device_sm_count();
+    const int grid = (int)std::min<int64_t>(items, sms > 0 ? sms : 1);
+    return launch_pdl(prefill_tc_kernel<T, D, G>, dim3(grid), dim3(kPfThreads), smem, st, qm, km, vm, p) ==
                    cudaSuccess
                ? PA_OK
                : PA_ERR_CUDA;
@@ -582,6 +783,7 @@ int launch_prefill(const PrefillArgs &a) {
     prm.num_blocks = a.num_blocks;
     prm.max_context_len = a.max_context_len;
     prm.num_tokens = a.num_tokens;
+    prm.num_seqs = a.num_seqs;
     prm.qk_scale_log2 = a.scale * kLog2e;
     prm.status = a.status;
     const int G = a.num_heads / a.num_kv_heads;

@@ -136,6 +136,28 @@ def test_prefill_shape_sweep(oracle_mod, dtype, D, G):
         check_case(case, oracle_mod)
 
 
+def test_prefill_unit_order_many_ragged_units(oracle_mod):
+    """60 sequences of random prefix and chunk lengths: the longest-first unit ranking
+    sees many ties and empty units and must still give every unit exactly one CTA set."""
+    rng = np.random.default_rng(21)
+    prefix = rng.integers(0, 3000, size=60).tolist()
+    chunk = rng.integers(1, 300, size=60).tolist()
+    case = workloads.make_prefill_case("pf-rank", prefix, chunk, 16, 16, 4, 128, torch.bfloat16,
+                                       seed=21)
+    check_case(case, oracle_mod)
+
+
+def test_prefill_unit_order_launch_order_fallback(oracle_mod):
+    """More than 4096 units (2100 sequences x 2 query tiles at G=1) skip the ranking and
+    run in launch order."""
+    prefix = [(7 * i) % 90 for i in range(2100)]
+    chunk = [1 + (i % 3) for i in range(2100)]
+    chunk[5] = 129  # two 128-row tiles
+    case = workloads.make_prefill_case("pf-many", prefix, chunk, 8, 2, 2, 64, torch.float16,
+                                       seed=22)
+    check_case(case, oracle_mod)
+
+
 def test_prefill_single_row_matches_decode(oracle_mod):
     """A chunk of one row is a decode step: both kernels agree within tolerance."""
     d = workloads.make_decode_case("pd", [63, 500, 1200], 16, 32, 8, 128, torch.bfloat16, 17)
