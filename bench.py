@@ -83,7 +83,7 @@ def kernel_source_hash(kind: str = "decode") -> str:
     """Hash of the CUDA sources a kernel is built from (ties ncu counters to a kernel version)."""
     csrc = ROOT / "paged_kv_attention_write_gb300" / "csrc"
     files = {"decode": ["decode.cu", "tma.cuh", "common.cuh"],
-             "prefill": ["prefill.cu", "common.cuh"]}[kind]
+             "prefill": ["prefill.cu", "tma.cuh", "common.cuh"]}[kind]
     h = hashlib.sha256()
     for f in files:
         h.update((csrc / f).read_bytes())

@@ -141,6 +141,13 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, ui
                  : "memory");
 }
 
+// max(a, b, c) in one instruction (returns the other operands when one is NaN)
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
 template <class T>
 __device__ __forceinline__ uint32_t pack2(float lo, float hi);
 template <>
@@ -153,17 +160,17 @@ __device__ __forceinline__ uint32_t pack2<F16>(float lo, float hi) {
     __half2 h = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&h);
 }
-// Sum of a packed pair as it enters the P.V product (numerator and denominator agree).
+// A packed pair widened to fp32 exactly as it enters the P.V product, so that the
+// row sum (denominator) adds the same rounded weights as the numerator.
 template <class T>
-__device__ __forceinline__ float unpack_sum(uint32_t u);
+__device__ __forceinline__ float2 unpack2(uint32_t u);
 template <>
-__device__ __forceinline__ float unpack_sum<BF16>(uint32_t u) {
-    return __uint_as_float(u << 16) + __uint_as_float(u & 0xffff0000u);
+__device__ __forceinline__ float2 unpack2<BF16>(uint32_t u) {
+    return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
 }
 template <>
-__device__ __forceinline__ float unpack_sum<F16>(uint32_t u) {
-    const float2 f = __half22float2(*reinterpret_cast<__half2 *>(&u));
-    return f.x + f.y;
+__device__ __forceinline__ float2 unpack2<F16>(uint32_t u) {
+    return __half22float2(*reinterpret_cast<__half2 *>(&u));
 }
 
 struct PrefillParams {
@@ -600,19 +607,24 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
                     }
                 }
                 // mask (keys k0 .. k0+lim-1 are visible; only the last tiles need it) and row
-                // max of the raw scores, in eight independent chains
+                // max of the raw scores, in eight independent chains of 3-input maxima
                 const int lim = min(pos + 1, it.C) - k0;
                 if (k0 + kBN > row0_pos + 1 || k0 + kBN > it.C) {  // tile-uniform
 #pragma unroll
                     for (int c = 0; c < kBN; ++c) sv[c] = c < lim ? sv[c] : -INFINITY;
                 }
+                static_assert(kBN == 128, "max tree layout");
                 float mx8[8];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) mx8[i] = sv[i];
+                for (int i = 0; i < 8; ++i) mx8[i] = fmax3(sv[i], sv[8 + i], sv[16 + i]);
 #pragma unroll
-                for (int c = 8; c < kBN; ++c) mx8[c % 8] = fmaxf(mx8[c % 8], sv[c]);
-                const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                                       fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) *
+                for (int c = 24; c + 16 <= kBN; c += 16)
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) mx8[i] = fmax3(mx8[i], sv[c + i], sv[c + 8 + i]);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) mx8[i] = fmaxf(mx8[i], sv[120 + i]);
+                const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
+                                       fmaxf(mx8[6], mx8[7])) *
                                  p.qk_scale_log2;
                 // lazy rescale; warp-uniform because the O row is read and written by the
                 // whole warp (tcgen05.ld / st)
@@ -639,21 +651,22 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
                 }
                 // P row over the S row just read: 128 keys packed two per TMEM column (the
                 // P.V of this buffer's previous tile finished before this S was issued)
-                const float sc = p.qk_scale_log2, neg_m = -m_ref;
-                float rs4[4] = {0.f, 0.f, 0.f, 0.f};
+                const float2 sc2 = make_float2(p.qk_scale_log2, p.qk_scale_log2), nm2 = make_float2(-m_ref, -m_ref);
+                float2 rs2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
                     uint32_t w[32];
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
                         const int c = half * 64 + 2 * i;
-                        w[i] = pack2<T>(fast_exp2(fmaf(sv[c], sc, neg_m)), fast_exp2(fmaf(sv[c + 1], sc, neg_m)));
-                        rs4[i & 3] += unpack_sum<T>(w[i]);
+                        const float2 x = __ffma2_rn(make_float2(sv[c], sv[c + 1]), sc2, nm2);
+                        w[i] = pack2<T>(fast_exp2(x.x), fast_exp2(x.y));
+                        rs2[i & 1] = __fadd2_rn(rs2[i & 1], unpack2<T>(w[i]));
                     }
                     tmem_st32(tS + half * 32, w);
                 }
                 tmem_wait_st();
-                l += (rs4[0] + rs4[1]) + (rs4[2] + rs4[3]);
+                l += (rs2[0].x + rs2[0].y) + (rs2[1].x + rs2[1].y);
                 // keys past kv_end in this tile (not loaded, or past the context): zero V rows,
                 // so that 0-weight rows never meet stale or NaN data
                 if (k0 + kBN > it.kv_end) {
