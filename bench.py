@@ -492,6 +492,49 @@ def gpu_arm(args, rank, world, dist_on):
     return line
 
 
+def mixed_batch_measurement(device, flush, hbm_peak, tc_peak):
+    """The mixed decode + prefill step as one pa_prefill_chunk launch, against the same rows
+    as two launches (pa_decode for the decode rows, pa_prefill_chunk for the chunks).  The
+    roofline time is the larger of FLOPs at the tensor peak and bytes at the HBM peak."""
+    import paged_kv_attention_write_gb300 as pa
+    case = workloads.mixed_batch()
+    nd = int(((case.query_start_loc[1:] - case.query_start_loc[:-1]) == 1).sum())
+    kc, vc = case.key_cache.to(device), case.value_cache.to(device)
+    pa.pa_reshape_and_cache(case.new_key.to(device), case.new_value.to(device), kc, vc,
+                            case.slot_mapping.to(device))
+    bt, cl = case.block_tables.to(device), case.context_lens.to(device)
+    q, qsl = case.query.to(device), case.query_start_loc.to(device)
+    out = torch.empty(tuple(q.shape), dtype=torch.float32, device=device)
+    mq = int((case.query_start_loc[1:] - case.query_start_loc[:-1]).max())
+    # the same rows split: decode rows (the first nd sequences) and the chunks
+    q_d, bt_d, cl_d = q[:nd], bt[:nd].contiguous(), cl[:nd].contiguous()
+    q_p, bt_p, cl_p = q[nd:], bt[nd:].contiguous(), cl[nd:].contiguous()
+    qsl_p = (qsl[nd:] - nd).contiguous()
+    out_d, out_p = torch.empty_like(out[:nd]), torch.empty_like(out[nd:])
+    ws = torch.empty(max(1, pa.pa_decode_workspace_size(nd, case.num_heads, case.num_kv_heads,
+                                                        case.head_dim, int(cl_d.max()))),
+                     dtype=torch.uint8, device=device)
+
+    def mixed():
+        pa.pa_prefill_chunk(out, q, qsl, mq, kc, vc, bt, cl, case.max_context_len, case.scale)
+
+    def split():
+        pa.pa_decode(out_d, q_d, kc, vc, bt_d, cl_d, int(cl_d.max()), case.scale, workspace=ws)
+        pa.pa_prefill_chunk(out_p, q_p, qsl_p, mq, kc, vc, bt_p, cl_p, case.max_context_len, case.scale)
+    for _ in range(5):
+        mixed()
+        split()
+    t_mix = statistics.mean(time_steps(mixed, 50, flush, False)[0])
+    t_split = statistics.mean(time_steps(split, 50, flush, False)[0])
+    flops, byts = prefill_work(case)
+    t_roof = max(flops / (tc_peak * 1e12), byts / (hbm_peak * 1e9)) * 1e3
+    return {"workload": case.name, "decode_rows": nd, "chunks": case.num_seqs - nd,
+            "ms_one_launch": round(t_mix, 5), "ms_decode_plus_prefill_launches": round(t_split, 5),
+            "tokens_per_s": round(int(q.shape[0]) / (t_mix * 1e-3), 1),
+            "TFLOP/s": round(flops / (t_mix * 1e-3) / 1e12, 1), "GB/s": round(byts / (t_mix * 1e-3) / 1e9, 1),
+            "roofline_ms": round(t_roof, 5), "frac_roofline": round(t_roof / t_mix, 4)}
+
+
 def secondary_measurements(device, flush, hbm_peak, tc_peak, peak_kind):
     """Shorter timings of the other hot-path rows: decode batch, chunked prefill, block copy."""
     import paged_kv_attention_write_gb300 as pa
@@ -537,6 +580,7 @@ def secondary_measurements(device, flush, hbm_peak, tc_peak, peak_kind):
     rb = nk.numel() * nk.element_size() * 4 + sl.numel() * 8
     res["reshape_and_cache_2048_tokens"] = {"ms": round(t, 5), "GB/s": round(rb / (t * 1e-3) / 1e9, 1)}
     del kc, vc
+    res["mixed_batch"] = mixed_batch_measurement(device, flush, hbm_peak, tc_peak)
     # block copy: 26 recipients' leading blocks of the stress workload (bs 16, bf16)
     case = workloads.stress_decode(block_size=16, dtype=torch.bfloat16)
     kc, vc = case.key_cache.to(device), case.value_cache.to(device)

@@ -158,6 +158,51 @@ def test_prefill_unit_order_launch_order_fallback(oracle_mod):
     check_case(case, oracle_mod)
 
 
+# ----------------------------------------------------------------------------- mixed decode + prefill batches
+
+def test_mixed_batch_full_size(oracle_mod):
+    """28 decode rows and four 512-token chunks in one pa_prefill_chunk launch."""
+    check_case(workloads.mixed_batch(), oracle_mod)
+
+
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16], ids=["fp16", "bf16"])
+@pytest.mark.parametrize("bs", [8, 32])
+def test_mixed_batch_interleaved(oracle_mod, dtype, bs):
+    """Decode rows between chunks (and a chunk on an empty prefix) in one launch."""
+    prefix = [300, 0, 47, 1000, 5, 129, 600]
+    chunk = [1, 200, 1, 64, 1, 1, 130]
+    case = workloads.make_prefill_case("mixed-il", prefix, chunk, bs, 16, 4, 128, dtype, seed=bs,
+                                       free_frac=0.1)
+    check_case(case, oracle_mod)
+
+
+def test_mixed_batch_decode_rows_match_alone_and_decode():
+    """Each item's arithmetic is independent of the others: the decode rows of a mixed
+    launch equal, bit for bit, the same rows run alone through pa_prefill_chunk, and
+    agree with pa_decode within tolerance."""
+    import paged_kv_attention_write_gb300 as pa
+    dev = "cuda"
+    mix = workloads.mixed_batch()
+    out_mix, kc, vc, st = gpu_step(mix)
+    assert st == 0
+    nd = 28  # decode rows come first, one query token each
+    q = mix.query[:nd].to(dev)
+    qsl = torch.arange(nd + 1, dtype=torch.int32, device=dev)
+    bt = mix.block_tables[:nd].contiguous().to(dev)
+    cl = mix.context_lens[:nd].contiguous().to(dev)
+    kc, vc = kc.to(dev), vc.to(dev)
+    alone = torch.empty(tuple(q.shape), dtype=torch.float32, device=dev)
+    pa.pa_prefill_chunk(alone, q, qsl, 1, kc, vc, bt, cl, int(cl.max()), mix.scale)
+    ws = torch.empty(max(1, pa.pa_decode_workspace_size(nd, mix.num_heads, mix.num_kv_heads,
+                                                        mix.head_dim, int(cl.max()))),
+                     dtype=torch.uint8, device=dev)
+    dec = torch.empty_like(alone)
+    pa.pa_decode(dec, q, kc, vc, bt, cl, int(cl.max()), mix.scale, workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(out_mix[:nd], alone.cpu())
+    assert (dec.cpu() - out_mix[:nd]).abs().max().item() < 5e-3
+
+
 def test_prefill_single_row_matches_decode(oracle_mod):
     """A chunk of one row is a decode step: both kernels agree within tolerance."""
     d = workloads.make_decode_case("pd", [63, 500, 1200], 16, 32, 8, 128, torch.bfloat16, 17)

@@ -35,7 +35,7 @@ import torch
 
 __all__ = [
     "PagedCase", "make_decode_case", "make_prefill_case", "tiny_decode", "decode_batch",
-    "long_decode", "prefill_chunk", "stress_decode", "WORKLOADS",
+    "long_decode", "prefill_chunk", "stress_decode", "mixed_batch", "WORKLOADS",
 ]
 
 
@@ -270,10 +270,24 @@ def stress_decode(block_size: int = 16, dtype: torch.dtype = torch.bfloat16, see
                             free_frac=0.2, share_frac=0.1)
 
 
+def mixed_batch(seed: int = 6) -> PagedCase:
+    """One mixed step in the vLLM v1 manner (Pure-Rust engines page, scheduling section:
+    prefill chunks and decode tokens share one batch under a token budget): 28 decode rows
+    (one new token on cached lengths uniform in [512, 4096]) followed by the four 512-token
+    chunks of the chunked-prefill workload; block 16, 32 q / 8 kv heads, D 128, bf16."""
+    rng = np.random.default_rng(1000 + seed)
+    dec = rng.integers(512, 4096, size=28, endpoint=True).tolist()
+    prefix = dec + [0, 1024, 2048, 3584]
+    chunk = [1] * 28 + [512] * 4
+    return make_prefill_case("mixed S32 28 decode rows L512-4096 + 4 chunks Q512 bs16 Hq32 Hkv8 D128 bf16",
+                             prefix, chunk, 16, 32, 8, 128, torch.bfloat16, seed)
+
+
 WORKLOADS = {
     "tiny_decode": tiny_decode,
     "decode_batch": decode_batch,
     "long_decode": long_decode,
     "prefill_chunk": prefill_chunk,
     "stress_decode": stress_decode,
+    "mixed_batch": mixed_batch,
 }
