@@ -29,6 +29,7 @@ import threading
 import time
 from pathlib import Path
 
+import numpy as np
 import torch
 
 ROOT = Path(__file__).resolve().parent
@@ -492,6 +493,81 @@ def gpu_arm(args, rank, world, dist_on):
     return line
 
 
+def manager_stream(seed: int = 9, num_requests: int = 400):
+    """A seeded serving-like stream of KV-cache manager calls: requests whose prompts start
+    with one of four system prompts (64-1024 tokens) plus their own text (16-1024 tokens),
+    at most 64 running at once; each running request takes one step per round (the next
+    512-token prefill chunk of its prompt, else one decode token), ceil(prompt / 512) + 32
+    steps, then it is freed.  Returns the calls: ("admit", id, tokens), ("step", id),
+    ("free", id)."""
+    rng = np.random.default_rng(seed)
+    systems = [rng.integers(0, 32000, size=int(rng.integers(64, 1025))).tolist() for _ in range(4)]
+    calls, running, nxt = [], {}, 0
+    while nxt < num_requests or running:
+        while nxt < num_requests and len(running) < 64:
+            toks = systems[int(rng.integers(4))] + rng.integers(0, 32000, size=int(rng.integers(16, 1025))).tolist()
+            calls.append(("admit", nxt, toks))
+            running[nxt] = -(-len(toks) // 512) + 32
+            nxt += 1
+        for rid in list(running):
+            calls.append(("step", rid))
+            running[rid] -= 1
+            if running[rid] == 0:
+                calls.append(("free", rid))
+                del running[rid]
+    return calls
+
+
+def replay_manager(mgr, calls, rng_seed: int = 1) -> int:
+    """Run a call stream on a manager (library or reference): admit, then per step allocate
+    the next prefill chunk (prompt tokens not yet computed, at most 512) or one decode token
+    and register full blocks, then free.  Tokens live in int32 arrays (no per-call list
+    conversion).  Returns the number of manager calls made."""
+    rng = np.random.default_rng(rng_seed)
+    state, n = {}, 0
+    for c in calls:
+        if c[0] == "admit":
+            _, rid, toks = c
+            buf = np.zeros(len(toks) + 64, dtype=np.int32)
+            buf[:len(toks)] = toks
+            state[rid] = [buf, mgr.admit(rid, buf[:len(toks)]), len(toks), len(toks)]
+            n += 1
+        elif c[0] == "step":
+            buf, done, plen, ntok = state[c[1]]
+            if done < plen:
+                new = min(plen, done + 512)
+            else:
+                buf[ntok] = int(rng.integers(32000))
+                ntok += 1
+                new = ntok
+            mgr.allocate_slots(c[1], new)
+            mgr.cache_blocks(c[1], buf[:ntok], new)
+            state[c[1]][1], state[c[1]][3] = new, ntok
+            n += 2
+        else:
+            mgr.free(c[1])
+            del state[c[1]]
+            n += 1
+    return n
+
+
+MANAGER_STREAM = "400 requests, 4 shared system prompts, 512-token chunks, 32 decode tokens, <= 64 running, bs 16, 16384 blocks"
+
+
+def manager_measurement():
+    """Host KV-cache manager (the library's C++ code): calls per second on a seeded
+    serving-like stream."""
+    from paged_kv_attention_write_gb300.kv_manager import KVCacheManager
+    calls = manager_stream()
+    mgr = KVCacheManager(16384, 16)
+    t0 = time.perf_counter()
+    n = replay_manager(mgr, calls)
+    dt = time.perf_counter() - t0
+    return {"stream": MANAGER_STREAM, "calls": n, "s": round(dt, 4), "calls_per_s": round(n / dt, 1),
+            "us_per_call": round(dt / n * 1e6, 3), "stats": mgr.stats(),
+            "note": "host time through the Python binding (ctypes marshalling included)"}
+
+
 def mixed_batch_measurement(device, flush, hbm_peak, tc_peak):
     """The mixed decode + prefill step as one pa_prefill_chunk launch, against the same rows
     as two launches (pa_decode for the decode rows, pa_prefill_chunk for the chunks).  The
@@ -581,6 +657,7 @@ def secondary_measurements(device, flush, hbm_peak, tc_peak, peak_kind):
     res["reshape_and_cache_2048_tokens"] = {"ms": round(t, 5), "GB/s": round(rb / (t * 1e-3) / 1e9, 1)}
     del kc, vc
     res["mixed_batch"] = mixed_batch_measurement(device, flush, hbm_peak, tc_peak)
+    res["kv_manager"] = manager_measurement()
     # block copy: 26 recipients' leading blocks of the stress workload (bs 16, bf16)
     case = workloads.stress_decode(block_size=16, dtype=torch.bfloat16)
     kc, vc = case.key_cache.to(device), case.value_cache.to(device)
@@ -619,7 +696,20 @@ def cpu_baseline(case, byts, reps: int = 2):
     t = statistics.median(times)
     return {"value": round(byts["step"] / t / 1e9, 4), "unit": "GB/s", "cores": oracle.num_threads(),
             "kind": "oracle", "seconds_per_step": round(t, 3),
-            "sample": f"{reps} whole steps of the same workload ({case.num_seqs} sequences, all heads), median"}
+            "sample": f"{reps} whole steps of the same workload ({case.num_seqs} sequences, all heads), median",
+            "kv_manager_reference": reference_manager_measurement()}
+
+
+def reference_manager_measurement():
+    """The reference KV-cache manager (plain Python) on the library manager's stream."""
+    from oracle.kv_manager import ReferenceKVManager
+    calls = manager_stream()
+    mgr = ReferenceKVManager(16384, 16)
+    t0 = time.perf_counter()
+    n = replay_manager(mgr, calls)
+    dt = time.perf_counter() - t0
+    return {"stream": MANAGER_STREAM, "calls": n, "s": round(dt, 4), "calls_per_s": round(n / dt, 1),
+            "cores": 1, "kind": "oracle"}
 
 
 def reference_arm(args, rank, world, budget_s: float = 150.0):

@@ -68,7 +68,8 @@ enum {
     PA_ERR_INVALID_ARG = -1, /* null / misaligned pointer, negative size, bad dtype */
     PA_ERR_UNSUPPORTED = -2, /* head_dim, block_size or head grouping not built */
     PA_ERR_WORKSPACE = -3,   /* workspace missing or smaller than required */
-    PA_ERR_CUDA = -4         /* a kernel launch failed (cudaGetLastError) */
+    PA_ERR_CUDA = -4,        /* a kernel launch failed (cudaGetLastError) */
+    PA_ERR_NO_BLOCKS = -5    /* KV-cache manager: not enough free blocks (nothing changed) */
 };
 
 /* Bits OR-ed into the optional device-side `*status` word. */

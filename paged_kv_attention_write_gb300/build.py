@@ -1,7 +1,7 @@
 """Build the in-tree CUDA library ``libpa.so`` for sm_103a with nvcc.
 
-Each ``csrc/*.cu`` translation unit is compiled in parallel, then linked into
-one shared library next to this file.  Object files go to ``_build/`` at the
+Each ``csrc/*.cu`` translation unit (and each host-only ``csrc/*.cpp`` one) is
+compiled in parallel, then linked into one shared library next to this file.  Object files go to ``_build/`` at the
 repository root.  ``python paged_kv_attention_write_gb300/build.py [-v]`` runs it (the
 package itself cannot be imported before the library exists).
 """
@@ -34,7 +34,7 @@ def nvcc() -> str:
 
 
 def _sources():
-    return sorted(CSRC.glob("*.cu"))
+    return sorted(CSRC.glob("*.cu")) + sorted(CSRC.glob("*.cpp"))
 
 
 def _deps():
@@ -57,7 +57,7 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> Path:
     flags = NVCC_FLAGS + list(extra_flags)
 
     def compile_one(src: Path) -> Path:
-        obj = BUILD / (src.stem + ".o")
+        obj = BUILD / (src.name.replace(".", "_") + ".o")
         cmd = [cc, *flags, "-c", str(src), "-o", str(obj)]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:

@@ -69,6 +69,7 @@ const char *pa_status_string(int code) {
         case PA_ERR_UNSUPPORTED: return "PA_ERR_UNSUPPORTED: head_dim, block_size, head grouping or dtype not built";
         case PA_ERR_WORKSPACE: return "PA_ERR_WORKSPACE: workspace missing, misaligned or too small";
         case PA_ERR_CUDA: return "PA_ERR_CUDA: kernel launch failed";
+        case PA_ERR_NO_BLOCKS: return "PA_ERR_NO_BLOCKS: not enough free KV-cache blocks";
     }
     return "unknown pa status code";
 }

@@ -16,14 +16,23 @@ def lib(pa_lib_path):
 
 
 def _declared_functions():
-    text = (ROOT / "include" / "pa.h").read_text()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(pa_\w+)\s*\(", text)))
+    names = set()
+    for h in sorted((ROOT / "include").glob("*.h")):
+        text = re.sub(r"/\*.*?\*/", "", h.read_text(), flags=re.S)
+        names |= set(re.findall(r"\b(pa_\w+)\s*\(", text))
+    return sorted(names)
 
 
 def test_header_declares_the_four_operations():
     names = _declared_functions()
     for op in ("pa_reshape_and_cache", "pa_decode", "pa_prefill_chunk", "pa_copy_blocks"):
+        assert op in names
+
+
+def test_headers_declare_the_kv_manager():
+    names = _declared_functions()
+    for op in ("pa_kvm_create", "pa_kvm_get_computed_blocks", "pa_kvm_allocate_slots",
+               "pa_kvm_cache_blocks", "pa_kvm_free"):
         assert op in names
 
 
@@ -34,7 +43,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 def test_status_strings_and_version(lib):
     lib.pa_status_string.restype = ctypes.c_char_p
-    for code in (0, -1, -2, -3, -4):
+    for code in (0, -1, -2, -3, -4, -5):
         assert lib.pa_status_string(code).startswith(b"PA_")
     assert lib.pa_status_string(12345) == b"unknown pa status code"
     assert lib.pa_version() >= 100
