@@ -568,6 +568,50 @@ def manager_measurement():
             "note": "host time through the Python binding (ctypes marshalling included)"}
 
 
+SERVE_REPLAY = ("256 requests at once: 70 % start with one of 4 system prompts (128-1024 tokens), "
+                "own text 64-1024 tokens, 32-256 generated tokens; 32 q / 8 kv heads, D 128, bs 16, bf16; "
+                "budget 4096 tokens, 512-token chunks, <= 8 decode steps in a row; q/k/v gathered from "
+                "seeded random tables by (token, position); one device read of each step's output")
+
+
+def serve_replay_measurement(device, num_requests: int = 256, seed: int = 11):
+    """The scheduler-driven replay (mistral.rs-style alternating prefill / decode steps)
+    through PagedAttentionEngine: host scheduling, one packed host-to-device copy, K/V write
+    and attention per step, one device read per step (the sampled tokens of a real engine
+    depend on it).  Reports generated tokens per second (seq-steps/s) end to end."""
+    from paged_kv_attention_write_gb300.engine import PagedAttentionEngine
+    rng = np.random.default_rng(seed)
+    Hq, Hkv, D, R = 32, 8, 128, 8192
+    g = torch.Generator().manual_seed(seed)
+    kt = torch.randn((R, Hkv, D), generator=g).to(torch.bfloat16).to(device)
+    vt = torch.randn((R, Hkv, D), generator=g).to(torch.bfloat16).to(device)
+    qt = torch.randn((R, Hq, D), generator=g).to(torch.bfloat16).to(device)
+    systems = [rng.integers(0, 32000, size=int(rng.integers(128, 1025))).tolist() for _ in range(4)]
+    eng = PagedAttentionEngine(40000, 16, Hq, Hkv, D, torch.bfloat16, device)
+    for rid in range(num_requests):
+        own = rng.integers(0, 32000, size=int(rng.integers(64, 1025))).tolist()
+        prompt = (systems[int(rng.integers(4))] + own) if rng.random() < 0.7 else own
+        eng.add_request(rid, prompt, int(rng.integers(32, 257)))
+    def qkv(step):
+        ids = (step["token_ids"].astype(np.int64) * 7919 + step["positions"].astype(np.int64) * 104729) % R
+        i = torch.from_numpy(ids).to(device, non_blocking=True)
+        return qt[i], kt[i], vt[i]
+
+    def sample(step, out):
+        out[:, 0, 0].cpu()  # the step's result reaches the host (a sampler would need it)
+        return rng.integers(0, 32000, size=step["num_seqs"])
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    steps = eng.run(qkv, sample)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    st, ms = eng.sched.stats(), eng.sched.manager_stats()
+    return {"workload": SERVE_REPLAY, "steps": steps, "s": round(wall, 3),
+            "seq_steps_per_s": round(st["generated_tokens"] / wall, 1),
+            "prompt_tokens_per_s": round(st["prefill_tokens"] / wall, 1),
+            "ms_per_step": round(wall / max(1, steps) * 1e3, 4), "scheduler": st, "kv_manager": ms}
+
+
 def mixed_batch_measurement(device, flush, hbm_peak, tc_peak):
     """The mixed decode + prefill step as one pa_prefill_chunk launch, against the same rows
     as two launches (pa_decode for the decode rows, pa_prefill_chunk for the chunks).  The
@@ -658,6 +702,7 @@ def secondary_measurements(device, flush, hbm_peak, tc_peak, peak_kind):
     del kc, vc
     res["mixed_batch"] = mixed_batch_measurement(device, flush, hbm_peak, tc_peak)
     res["kv_manager"] = manager_measurement()
+    res["serve_replay"] = serve_replay_measurement(device)
     # block copy: 26 recipients' leading blocks of the stress workload (bs 16, bf16)
     case = workloads.stress_decode(block_size=16, dtype=torch.bfloat16)
     kc, vc = case.key_cache.to(device), case.value_cache.to(device)

@@ -55,6 +55,19 @@ class ReferenceKVManager:
         self.hits += len(hits)
         return hits
 
+    def peek_hits(self, tokens: Sequence[int]) -> List[int]:
+        """The blocks a lookup would hit, without counting a lookup."""
+        if not self.prefix_cache or len(tokens) <= 1:
+            return []
+        tokens = list(tokens)
+        hits = []
+        for i in range((len(tokens) - 1) // self.bs):
+            key = tuple(tokens[:(i + 1) * self.bs])
+            if key not in self.cache:
+                break
+            hits.append(self.cache[key])
+        return hits
+
     def _take_head(self) -> int:
         b = self.free_queue.pop(0)
         if b in self.prefix_of:  # a cached block handed out again leaves the cache
