@@ -211,6 +211,65 @@ int pa_copy_blocks(void *key_cache, void *value_cache, const int64_t *block_mapp
                    int num_kv_heads, int head_dim, int block_size, int num_blocks,
                    pa_dtype kv_dtype, int32_t *status, pa_stream_t stream);
 
+/*
+ * Rotary position embedding fused into the cache write and the decode query load
+ * (TensorSharp "Mistral 3" page, section 3 "Forward graph" and section 4.2 "RoPE - GPT-J
+ * style with YaRN": RoPE rotates Q and K with the GPT-J pairing -- adjacent elements
+ * (x[2i], x[2i+1]) rotate together -- at each token's absolute position, with a frequency
+ * table built once at load time (YaRN-corrected when the model asks for it); Q is then
+ * scaled by 1 + beta * log(1 + floor(pos / origCtx)) when origCtx > 0).
+ *
+ * Pair i (i < rope_dim / 2) of a row at position pos is rotated by the angle
+ * pos * freqs[i]:  (x, y) -> (x cos - y sin, x sin + y cos).  The angle is formed and
+ * reduced to [-pi, pi] in double, its sine and cosine taken in fp32 (absolute error below
+ * 4e-7), the rotation done in fp32.  Elements past rope_dim are not rotated.  The 1/sqrt(head_dim) factor stays the attention's `scale` argument.
+ */
+typedef struct {
+    const float *freqs;   /* device, [rope_dim / 2]: angular frequency of pair i (pa_rope_yarn_freqs) */
+    int rope_dim;         /* even, 2 .. head_dim */
+    float q_scale_beta;   /* beta of the position-dependent query scale */
+    int q_scale_orig_ctx; /* origCtx of the query scale; 0 turns the scale off */
+} pa_rope;
+
+/*
+ * pa_rope_yarn_freqs -- host: the frequency table, freqs[i] = base^(-2i / rope_dim), then
+ * YaRN-corrected when yarn_scale != 1 and orig_ctx > 0 (section 4.2): with r = orig_ctx /
+ * (2 pi / f), the number of turns pair i makes over the original context, a pair with
+ * r > beta_fast keeps f (extrapolation), one with r < beta_slow takes f / yarn_scale
+ * (interpolation), and in between f mixes linearly in r: f * (1 - g) + f / yarn_scale * g
+ * with g = (beta_fast - r) / (beta_fast - beta_slow).  Computed in double, stored fp32.
+ * freqs: host array of rope_dim / 2 floats.
+ */
+int pa_rope_yarn_freqs(float *freqs, int rope_dim, float base, float yarn_scale, int orig_ctx,
+                       float beta_fast, float beta_slow);
+
+/*
+ * pa_reshape_and_cache_rope -- pa_reshape_and_cache with K rotated on the way in:
+ * token t's key row is rotated at position positions[t] (int32 [num_tokens], device)
+ * before it is written; values are copied as they are.  Same layouts, skip rule and errors
+ * as pa_reshape_and_cache, plus PA_ERR_INVALID_ARG for a missing rope/positions/freqs, an
+ * odd rope_dim or one outside 2..head_dim.
+ */
+int pa_reshape_and_cache_rope(const void *key, const void *value, void *key_cache, void *value_cache,
+                              const int64_t *slot_mapping, const int32_t *positions, int num_tokens,
+                              int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                              pa_dtype kv_dtype, const pa_rope *rope, int32_t *status,
+                              pa_stream_t stream);
+
+/*
+ * pa_decode_rope -- pa_decode with the query rotated and scaled as it is loaded: the query
+ * of sequence s sits at position context_lens[s] - 1 (the newest token), is rotated there
+ * and, when q_scale_orig_ctx > 0, multiplied by 1 + q_scale_beta * log(1 + floor(pos /
+ * q_scale_orig_ctx)); `query` holds the unrotated query.  Keys must already be rotated in
+ * the cache (pa_reshape_and_cache_rope).  Arguments otherwise as pa_decode.
+ */
+int pa_decode_rope(void *out, pa_dtype out_dtype, const void *query, const void *key_cache,
+                   const void *value_cache, const int32_t *block_tables, int max_blocks_per_seq,
+                   const int32_t *context_lens, int max_context_len, int num_seqs, int num_heads,
+                   int num_kv_heads, int head_dim, int block_size, int num_blocks, float scale,
+                   pa_dtype kv_dtype, const pa_rope *rope, void *workspace, size_t workspace_bytes,
+                   int32_t *status, pa_stream_t stream);
+
 /* Static description of a PA_* return code. */
 const char *pa_status_string(int code);
 

@@ -12,7 +12,10 @@ Operations (see ``include/pa.h`` for layouts, ownership and error behaviour):
 * ``pa_reshape_and_cache`` -- write fresh K/V to their cache slots;
 * ``pa_decode`` -- one query token per sequence, split-K + log-sum-exp reduce;
 * ``pa_prefill_chunk`` -- chunked prefill, causal in the chunk, full over the prefix;
-* ``pa_copy_blocks`` -- whole-block copies for prefix-cache reuse.
+* ``pa_copy_blocks`` -- whole-block copies for prefix-cache reuse;
+* ``pa_reshape_and_cache_rope`` / ``pa_decode_rope`` -- the same with rotary position
+  embedding (GPT-J pairs, YaRN table from ``pa_rope_yarn_freqs``) fused into the key write
+  and the decode query load.
 """
 from __future__ import annotations
 
@@ -25,6 +28,7 @@ import torch
 __all__ = [
     "PAError", "pa_reshape_and_cache", "pa_decode_workspace_size", "pa_decode", "pa_decode_noalloc",
     "pa_prefill_chunk", "pa_copy_blocks", "pa_status_string", "pa_version", "library_path",
+    "Rope", "pa_rope_yarn_freqs", "pa_reshape_and_cache_rope", "pa_decode_rope",
     "PA_F32", "PA_F16", "PA_BF16",
 ]
 
@@ -53,8 +57,20 @@ _lib.pa_copy_blocks.argtypes = [_vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i3
 _lib.pa_status_string.argtypes = [_i32]
 _lib.pa_status_string.restype = ctypes.c_char_p
 _lib.pa_version.argtypes = []
+
+
+class _PaRope(ctypes.Structure):
+    _fields_ = [("freqs", _vp), ("rope_dim", _i32), ("q_scale_beta", _f32), ("q_scale_orig_ctx", _i32)]
+
+
+_lib.pa_rope_yarn_freqs.argtypes = [_vp, _i32, _f32, _f32, _i32, _f32, _f32]
+_lib.pa_reshape_and_cache_rope.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32,
+                                           ctypes.POINTER(_PaRope), _vp, _vp]
+_lib.pa_decode_rope.argtypes = [_vp, _i32, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32,
+                                _i32, _i32, _f32, _i32, ctypes.POINTER(_PaRope), _vp, _sz, _vp, _vp]
 for _name in ("pa_reshape_and_cache", "pa_decode", "pa_decode_noalloc", "pa_prefill_chunk",
-              "pa_copy_blocks", "pa_version"):
+              "pa_copy_blocks", "pa_version", "pa_rope_yarn_freqs", "pa_reshape_and_cache_rope",
+              "pa_decode_rope"):
     getattr(_lib, _name).restype = _i32
 
 
@@ -163,3 +179,54 @@ def pa_copy_blocks(key_cache, value_cache, block_mapping, *, status=None, stream
     _check(_lib.pa_copy_blocks(_ptr(key_cache), _ptr(value_cache), _ptr(block_mapping),
                                block_mapping.shape[0], Hkv, D, bs, NB, _dt(key_cache),
                                _ptr(status), _stream(stream)), "pa_copy_blocks")
+
+
+# ----------------------------------------------------------------------------- rotary embedding
+
+def pa_rope_yarn_freqs(rope_dim: int, base: float, yarn_scale: float = 1.0, orig_ctx: int = 0,
+                       beta_fast: float = 32.0, beta_slow: float = 1.0):
+    """The RoPE frequency table (host, fp32 ``[rope_dim / 2]``), YaRN-corrected when
+    ``yarn_scale != 1`` and ``orig_ctx > 0`` (``include/pa.h`` states the formula)."""
+    import numpy as np
+    out = np.empty(rope_dim // 2, dtype=np.float32)
+    _check(_lib.pa_rope_yarn_freqs(out.ctypes.data, rope_dim, float(base), float(yarn_scale), int(orig_ctx),
+                                   float(beta_fast), float(beta_slow)), "pa_rope_yarn_freqs")
+    return out
+
+
+class Rope:
+    """Rotary-embedding arguments: ``freqs`` a device fp32 tensor ``[rope_dim / 2]``, the
+    rotated width, and the position-dependent query scale (off when ``q_scale_orig_ctx`` is 0)."""
+
+    def __init__(self, freqs: torch.Tensor, rope_dim: int, q_scale_beta: float = 0.0, q_scale_orig_ctx: int = 0):
+        self.freqs, self.rope_dim = freqs, rope_dim
+        self.q_scale_beta, self.q_scale_orig_ctx = q_scale_beta, q_scale_orig_ctx
+
+    def _c(self):
+        return _PaRope(self.freqs.data_ptr(), int(self.rope_dim), float(self.q_scale_beta), int(self.q_scale_orig_ctx))
+
+
+def pa_reshape_and_cache_rope(key, value, key_cache, value_cache, slot_mapping, positions, rope: Rope, *,
+                              status=None, stream=None) -> None:
+    """pa_reshape_and_cache with each key row rotated at ``positions`` (int32 [T])."""
+    T, Hkv, D = key.shape
+    NB, bs = key_cache.shape[:2]
+    r = rope._c()
+    _check(_lib.pa_reshape_and_cache_rope(_ptr(key), _ptr(value), _ptr(key_cache), _ptr(value_cache),
+                                          _ptr(slot_mapping), _ptr(positions), T, Hkv, D, bs, NB,
+                                          _dt(key_cache), ctypes.byref(r), _ptr(status), _stream(stream)),
+           "pa_reshape_and_cache_rope")
+
+
+def pa_decode_rope(out, query, key_cache, value_cache, block_tables, context_lens, max_context_len: int,
+                   scale: float, rope: Rope, *, workspace=None, status=None, stream=None) -> None:
+    """pa_decode with the (unrotated) query rotated and scaled at position context_len - 1."""
+    S, Hq, D = query.shape
+    NB, bs, Hkv, _ = key_cache.shape
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    r = rope._c()
+    _check(_lib.pa_decode_rope(_ptr(out), _dt(out), _ptr(query), _ptr(key_cache), _ptr(value_cache),
+                               _ptr(block_tables), block_tables.shape[1], _ptr(context_lens),
+                               int(max_context_len), S, Hq, Hkv, D, bs, NB, float(scale), _dt(key_cache),
+                               ctypes.byref(r), _ptr(workspace), ws_bytes, _ptr(status), _stream(stream)),
+           "pa_decode_rope")

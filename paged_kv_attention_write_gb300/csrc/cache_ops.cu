@@ -8,7 +8,8 @@
 //   page, block-hash prefix cache).  A block is bs*Hkv*D contiguous elements.
 //
 // Both are HBM-bound bit copies: 16-byte vector loads and stores, coalesced
-// along the row; no arithmetic on the elements.
+// along the row; no arithmetic on the elements.  A third kernel writes the cache with
+// the key rotated (RoPE) on the way in.
 #include "common.cuh"
 
 namespace pa {
@@ -71,7 +72,120 @@ copy_blocks_kernel(uint4 *__restrict__ key_cache, uint4 *__restrict__ value_cach
     }
 }
 
+// reshape_and_cache with the key rotated on the way in (RoPE, GPT-J pairing: TensorSharp
+// "Mistral 3" page, section 4.2).  One CTA per token: the token's cos/sin of every pair
+// are computed once into shared memory and shared by its kv heads; each thread
+// then rotates 16-byte vectors of the key row in fp32 and writes them, and copies the
+// value row.  T is the element type of the cache (F32, F16, BF16 tags).
+constexpr int kRopeMaxPairs = 64;  // rope_dim <= head_dim <= 128
+
+template <class T>
+__device__ __forceinline__ uint4 narrow16(const float *f);
+template <>
+__device__ __forceinline__ uint4 narrow16<F32>(const float *f) {
+    return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]), __float_as_uint(f[3]));
+}
+template <>
+__device__ __forceinline__ uint4 narrow16<BF16>(const float *f) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+        w[i] = *reinterpret_cast<uint32_t *>(&h);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+template <>
+__device__ __forceinline__ uint4 narrow16<F16>(const float *f) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        __half2 h = __floats2half2_rn(f[2 * i], f[2 * i + 1]);
+        w[i] = *reinterpret_cast<uint32_t *>(&h);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+template <class T>
+__global__ void __launch_bounds__(kCopyThreads)
+reshape_and_cache_rope_kernel(const uint4 *__restrict__ key, const uint4 *__restrict__ value,
+                              uint4 *__restrict__ key_cache, uint4 *__restrict__ value_cache,
+                              const int64_t *__restrict__ slot_mapping, const int32_t *__restrict__ positions,
+                              const float *__restrict__ freqs, int rope_dim, int head_dim, int vecs_per_row,
+                              int64_t num_slots, int32_t *status) {
+    constexpr int EPV = T::kPerVec;  // elements per 16-byte vector
+    __shared__ float2 cs[kRopeMaxPairs];                          // (cos, sin) of each pair
+    pdl_wait_previous();
+    pdl_launch_dependents();
+    const int t = blockIdx.x;
+    const int64_t slot = slot_mapping[t];
+    if (slot < 0) return;  // padding token
+    if (slot >= num_slots) {
+        if (threadIdx.x == 0) report(status, PA_DEVERR_SLOT);
+        return;
+    }
+    const int pos = positions[t];
+    for (int i = threadIdx.x; i < rope_dim / 2; i += kCopyThreads) cs[i] = rope_cos_sin(pos, freqs[i]);
+    __syncthreads();
+    const uint4 *ks = key + (int64_t)t * vecs_per_row;
+    const uint4 *vs = value + (int64_t)t * vecs_per_row;
+    uint4 *kd = key_cache + slot * vecs_per_row;
+    uint4 *vd = value_cache + slot * vecs_per_row;
+    for (int i = threadIdx.x; i < vecs_per_row; i += kCopyThreads) {
+        const int d0 = (i * EPV) % head_dim;  // first element of the vector within its head
+        uint4 k = ks[i];
+        if (d0 < rope_dim) {
+            float f[EPV];
+            widen(T{}, k, f);
+#pragma unroll
+            for (int e = 0; e < EPV; e += 2) {
+                const int pair = (d0 + e) / 2;
+                if (2 * pair < rope_dim) {
+                    const float2 r = cs[pair];
+                    const float x = f[e], y = f[e + 1];
+                    f[e] = x * r.x - y * r.y;
+                    f[e + 1] = x * r.y + y * r.x;
+                }
+            }
+            k = narrow16<T>(f);
+        }
+        kd[i] = k;
+        vd[i] = vs[i];
+    }
+}
+
 }  // namespace
+
+int launch_reshape_and_cache_rope(const void *key, const void *value, void *key_cache, void *value_cache,
+                                  const int64_t *slot_mapping, const int32_t *positions, int num_tokens,
+                                  int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                                  pa_dtype kv_dtype, const float *freqs, int rope_dim, int32_t *status,
+                                  cudaStream_t stream) {
+    if (num_tokens == 0) return PA_OK;
+    const int eb = kv_dtype == PA_F32 ? 4 : 2;
+    const int vecs = num_kv_heads * head_dim * eb / 16;
+    const int64_t slots = (int64_t)num_blocks * block_size;
+    const uint4 *k = static_cast<const uint4 *>(key), *v = static_cast<const uint4 *>(value);
+    uint4 *kc = static_cast<uint4 *>(key_cache), *vc = static_cast<uint4 *>(value_cache);
+    cudaError_t e;
+    switch (kv_dtype) {
+        case PA_F32:
+            e = launch_pdl(reshape_and_cache_rope_kernel<F32>, dim3(num_tokens), dim3(kCopyThreads), 0, stream, k,
+                           v, kc, vc, slot_mapping, positions, freqs, rope_dim, head_dim, vecs, slots, status);
+            break;
+        case PA_F16:
+            e = launch_pdl(reshape_and_cache_rope_kernel<F16>, dim3(num_tokens), dim3(kCopyThreads), 0, stream, k,
+                           v, kc, vc, slot_mapping, positions, freqs, rope_dim, head_dim, vecs, slots, status);
+            break;
+        case PA_BF16:
+            e = launch_pdl(reshape_and_cache_rope_kernel<BF16>, dim3(num_tokens), dim3(kCopyThreads), 0, stream, k,
+                           v, kc, vc, slot_mapping, positions, freqs, rope_dim, head_dim, vecs, slots, status);
+            break;
+        default:
+            return PA_ERR_UNSUPPORTED;
+    }
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
 
 int launch_reshape_and_cache(const void *key, const void *value, void *key_cache,
                              void *value_cache, const int64_t *slot_mapping, int num_tokens,

@@ -97,6 +97,20 @@ __device__ __forceinline__ float fast_exp2(float x) {
     return y;
 }
 
+// (cos, sin) of the RoPE angle pos * f: the angle is reduced to about [-pi, pi] in double
+// (one 2 pi constant: the reduced angle is off by under 1e-10 for |pos * f| < 1e6), then
+// __sincosf on the reduced angle (absolute error below 4e-7, far under the bf16 / fp16
+// resolution of the rotated values).
+__device__ __forceinline__ float2 rope_cos_sin(int pos, float f) {
+    constexpr double kTwoPi = 6.283185307179586476925286766559;
+    constexpr double kInvTwoPi = 0.15915494309189533576888376337251;
+    const double a = (double)pos * (double)f;
+    const double k = rint(a * kInvTwoPi);
+    float s, c;
+    __sincosf((float)fma(-k, kTwoPi, a), &s, &c);
+    return make_float2(c, s);
+}
+
 __device__ __forceinline__ void report(int32_t *status, int bit) {
     if (status) atomicOr(status, bit);
 }
@@ -153,6 +167,11 @@ struct DecodeArgs {
     size_t workspace_bytes;
     int32_t *status;
     cudaStream_t stream;
+    // query RoPE and position-dependent scale (null freqs: none)
+    const float *rope_freqs = nullptr;
+    int rope_dim = 0;
+    float q_scale_beta = 0.f;
+    int q_scale_orig_ctx = 0;
 };
 
 struct PrefillArgs {
@@ -178,6 +197,11 @@ int launch_reshape_and_cache(const void *key, const void *value, void *key_cache
                              void *value_cache, const int64_t *slot_mapping, int num_tokens,
                              int row_bytes, int block_size, int num_blocks, int32_t *status,
                              cudaStream_t stream);
+int launch_reshape_and_cache_rope(const void *key, const void *value, void *key_cache, void *value_cache,
+                                  const int64_t *slot_mapping, const int32_t *positions, int num_tokens,
+                                  int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                                  pa_dtype kv_dtype, const float *freqs, int rope_dim, int32_t *status,
+                                  cudaStream_t stream);
 int launch_copy_blocks(void *key_cache, void *value_cache, const int64_t *block_mapping,
                        int num_pairs, int64_t block_bytes, int num_blocks, int32_t *status,
                        cudaStream_t stream);

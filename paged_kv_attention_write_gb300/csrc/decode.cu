@@ -95,6 +95,11 @@ struct DecodeParams {
     int grid;             // CTAs launched for the split kernel
     float qk_scale_log2;  // scale * log2(e)
     int32_t *status;
+    // query RoPE (GPT-J pairs) and position-dependent scale, at position context_len - 1
+    const float *rope_freqs;  // null: no rotation, no scale
+    int rope_dim;
+    float q_scale_beta;
+    int q_scale_orig_ctx;
 };
 
 // ------------------------------------------------------------------------------ helpers
@@ -498,12 +503,34 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
         for (int hh = 0; hh < G; ++hh) {
             const uint4 raw = *reinterpret_cast<const uint4 *>(qp + hh * D);
             widen_vec<T>(raw, q2[hh]);
+        }
+        float qs = p.qk_scale_log2;
+        if (p.rope_freqs) {
+            // RoPE at the newest token's position (GPT-J pairs: this lane's float2 entries are
+            // the pairs (2i, 2i+1), i = r * EPV / 2 + e)
+            const int pos = max(p.context_lens[s] - 1, 0);
 #pragma unroll
             for (int e = 0; e < EPV / 2; ++e) {
-                q2[hh][e].x *= p.qk_scale_log2;
-                q2[hh][e].y *= p.qk_scale_log2;
+                const int pair = r * (EPV / 2) + e;
+                if (2 * pair < p.rope_dim) {
+                    const float2 cs = rope_cos_sin(pos, p.rope_freqs[pair]);
+#pragma unroll
+                    for (int hh = 0; hh < G; ++hh) {
+                        const float x = q2[hh][e].x, y = q2[hh][e].y;
+                        q2[hh][e] = make_float2(x * cs.x - y * cs.y, x * cs.y + y * cs.x);
+                    }
+                }
             }
+            if (p.q_scale_orig_ctx > 0)
+                qs *= (float)(1.0 + (double)p.q_scale_beta * log1p((double)(pos / p.q_scale_orig_ctx)));
         }
+#pragma unroll
+        for (int hh = 0; hh < G; ++hh)
+#pragma unroll
+            for (int e = 0; e < EPV / 2; ++e) {
+                q2[hh][e].x *= qs;
+                q2[hh][e].y *= qs;
+            }
     };
 
     // One stage: NT tokens of kv head h starting at logical token `tok0`.
@@ -870,6 +897,10 @@ int launch_decode(const DecodeArgs &a) {
     prm.grid = L.C;
     prm.qk_scale_log2 = a.scale * kLog2e;
     prm.status = a.status;
+    prm.rope_freqs = a.rope_freqs;
+    prm.rope_dim = a.rope_dim;
+    prm.q_scale_beta = a.q_scale_beta;
+    prm.q_scale_orig_ctx = a.q_scale_orig_ctx;
 
     // box rows are set per instantiation (they depend on the stage shape); encode the
     // tensor maps with the largest box the shape can use and re-encode if smaller.

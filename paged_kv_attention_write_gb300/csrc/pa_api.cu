@@ -138,6 +138,62 @@ int pa_decode(void *out, pa_dtype out_dtype, const void *query, const void *key_
     return pa::launch_decode(a);
 }
 
+// The rotary-embedding arguments shared by the two fused entry points.
+static int check_rope(const pa_rope *rope, int head_dim) {
+    if (!rope || !rope->freqs || !aligned(rope->freqs, 4)) return PA_ERR_INVALID_ARG;
+    if (rope->rope_dim < 2 || rope->rope_dim % 2 != 0 || rope->rope_dim > head_dim) return PA_ERR_INVALID_ARG;
+    if (rope->q_scale_orig_ctx < 0) return PA_ERR_INVALID_ARG;
+    return PA_OK;
+}
+
+int pa_decode_rope(void *out, pa_dtype out_dtype, const void *query, const void *key_cache,
+                   const void *value_cache, const int32_t *block_tables, int max_blocks_per_seq,
+                   const int32_t *context_lens, int max_context_len, int num_seqs, int num_heads,
+                   int num_kv_heads, int head_dim, int block_size, int num_blocks, float scale,
+                   pa_dtype kv_dtype, const pa_rope *rope, void *workspace, size_t workspace_bytes,
+                   int32_t *status, pa_stream_t stream) {
+    int rc = check_attention(out, out_dtype, query, key_cache, value_cache, block_tables,
+                             max_blocks_per_seq, context_lens, max_context_len, num_seqs,
+                             num_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,
+                             kv_dtype);
+    if (rc != PA_OK) return rc;
+    if ((rc = check_rope(rope, head_dim)) != PA_OK) return rc;
+    if (num_seqs == 0) return PA_OK;
+    if (!aligned(status, 4)) return PA_ERR_INVALID_ARG;
+    if (!workspace || !aligned(workspace, 16)) return PA_ERR_WORKSPACE;
+    pa::DecodeArgs a{out,          out_dtype,      query,     key_cache,    value_cache,
+                     block_tables, max_blocks_per_seq, context_lens, max_context_len,
+                     num_seqs,     num_heads,      num_kv_heads, head_dim,  block_size,
+                     num_blocks,   scale,          kv_dtype,  workspace,    workspace_bytes,
+                     status,       reinterpret_cast<cudaStream_t>(stream)};
+    a.rope_freqs = rope->freqs;
+    a.rope_dim = rope->rope_dim;
+    a.q_scale_beta = rope->q_scale_beta;
+    a.q_scale_orig_ctx = rope->q_scale_orig_ctx;
+    return pa::launch_decode(a);
+}
+
+int pa_reshape_and_cache_rope(const void *key, const void *value, void *key_cache, void *value_cache,
+                              const int64_t *slot_mapping, const int32_t *positions, int num_tokens,
+                              int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                              pa_dtype kv_dtype, const pa_rope *rope, int32_t *status,
+                              pa_stream_t stream) {
+    const int eb = elem_bytes(kv_dtype);
+    if (!eb || num_tokens < 0 || num_kv_heads <= 0 || num_blocks < 0) return PA_ERR_INVALID_ARG;
+    if (!head_dim_ok(head_dim) || !block_size_ok(block_size)) return PA_ERR_UNSUPPORTED;
+    int rc = check_rope(rope, head_dim);
+    if (rc != PA_OK) return rc;
+    if (num_tokens == 0) return PA_OK;
+    if (!key || !value || !key_cache || !value_cache || !slot_mapping || !positions) return PA_ERR_INVALID_ARG;
+    if (!aligned(key, 16) || !aligned(value, 16) || !aligned(key_cache, 16) || !aligned(value_cache, 16) ||
+        !aligned(slot_mapping, 8) || !aligned(positions, 4) || !aligned(status, 4))
+        return PA_ERR_INVALID_ARG;
+    return pa::launch_reshape_and_cache_rope(key, value, key_cache, value_cache, slot_mapping, positions,
+                                             num_tokens, num_kv_heads, head_dim, block_size, num_blocks,
+                                             kv_dtype, rope->freqs, rope->rope_dim, status,
+                                             reinterpret_cast<cudaStream_t>(stream));
+}
+
 int pa_prefill_chunk(void *out, pa_dtype out_dtype, const void *query,
                      const int32_t *query_start_loc, int num_tokens, int max_query_len,
                      const void *key_cache, const void *value_cache, const int32_t *block_tables,
