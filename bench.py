@@ -83,7 +83,7 @@ def prefill_work(case) -> tuple[float, int]:
 def kernel_source_hash(kind: str = "decode") -> str:
     """Hash of the CUDA sources a kernel is built from (ties ncu counters to a kernel version)."""
     csrc = ROOT / "paged_kv_attention_write_gb300" / "csrc"
-    files = {"decode": ["decode.cu", "tma.cuh", "common.cuh"],
+    files = {"decode": ["decode_kernels.cuh", "decode.cu", "tma.cuh", "common.cuh"],
              "prefill": ["prefill.cu", "tma.cuh", "common.cuh"]}[kind]
     h = hashlib.sha256()
     for f in files:
@@ -630,6 +630,44 @@ def serve_replay_measurement(device, num_requests: int = 256, seed: int = 11):
             "scheduler": st, "kv_manager": ms, "warmup": "one untimed replay of the same workload"}
 
 
+def rope_measurement(device, flush, hbm_peak):
+    """The fused rotary-embedding entry points beside their plain counterparts on the same
+    data: the chunked-prefill workload's 2048-token cache write, and decode on the
+    decode-batch workload (its query rotated and scaled at each sequence's position)."""
+    import paged_kv_attention_write_gb300 as pa
+    res = {}
+    freqs = torch.from_numpy(pa.pa_rope_yarn_freqs(128, 1e6, 8.0, 4096, 32.0, 1.0)).to(device)
+    rope = pa.Rope(freqs, 128, 0.1, 4096)
+    case = workloads.prefill_chunk()
+    kc, vc = case.key_cache.to(device), case.value_cache.to(device)
+    nk, nv, sl = case.new_key.to(device), case.new_value.to(device), case.slot_mapping.to(device)
+    qsl = case.query_start_loc.tolist()
+    pos = torch.tensor(sum((list(range(int(case.context_lens[s]) - (qsl[s + 1] - qsl[s]), int(case.context_lens[s])))
+                            for s in range(case.num_seqs)), []), dtype=torch.int32, device=device)
+    rb = nk.numel() * nk.element_size() * 4 + sl.numel() * 8 + pos.numel() * 4
+    for name, fn in (("reshape_and_cache", lambda: pa.pa_reshape_and_cache(nk, nv, kc, vc, sl)),
+                     ("reshape_and_cache_rope", lambda: pa.pa_reshape_and_cache_rope(nk, nv, kc, vc, sl, pos, rope))):
+        for _ in range(3):
+            fn()
+        t = statistics.mean(time_steps(fn, 50, flush, False)[0])
+        res[name + "_2048_tokens"] = {"ms": round(t, 5), "GB/s": round(rb / (t * 1e-3) / 1e9, 1)}
+    del kc, vc
+    case = workloads.decode_batch()
+    st = DecodeStep(case, device)
+    st.reshape()
+    b = decode_bytes(case)["decode"]
+    for name, fn in (("decode", st.decode),
+                     ("decode_rope", lambda: pa.pa_decode_rope(st.out, st.q, st.kc, st.vc, st.bt, st.cl, st.max_ctx,
+                                                               case.scale, rope, workspace=st.ws))):
+        for _ in range(3):
+            fn()
+        t = statistics.mean(time_steps(fn, 50, flush, False)[0])
+        res[name + "_decode_batch"] = {"ms": round(t, 5), "GB/s": round(b / t / 1e6, 1),
+                                       "frac_hbm": round(b / t / 1e6 / hbm_peak, 4)}
+    res["workloads"] = "cache write: prefill_chunk's 2048 tokens; decode: decode_batch (32 sequences)"
+    return res
+
+
 def mixed_batch_measurement(device, flush, hbm_peak, tc_peak):
     """The mixed decode + prefill step as one pa_prefill_chunk launch, against the same rows
     as two launches (pa_decode for the decode rows, pa_prefill_chunk for the chunks).  The
@@ -718,6 +756,7 @@ def secondary_measurements(device, flush, hbm_peak, tc_peak, peak_kind):
     rb = nk.numel() * nk.element_size() * 4 + sl.numel() * 8
     res["reshape_and_cache_2048_tokens"] = {"ms": round(t, 5), "GB/s": round(rb / (t * 1e-3) / 1e9, 1)}
     del kc, vc
+    res["rope"] = rope_measurement(device, flush, hbm_peak)
     res["mixed_batch"] = mixed_batch_measurement(device, flush, hbm_peak, tc_peak)
     res["kv_manager"] = manager_measurement()
     res["serve_replay"] = serve_replay_measurement(device)

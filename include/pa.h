@@ -220,9 +220,12 @@ int pa_copy_blocks(void *key_cache, void *value_cache, const int64_t *block_mapp
  * scaled by 1 + beta * log(1 + floor(pos / origCtx)) when origCtx > 0).
  *
  * Pair i (i < rope_dim / 2) of a row at position pos is rotated by the angle
- * pos * freqs[i]:  (x, y) -> (x cos - y sin, x sin + y cos).  The angle is formed and
- * reduced to [-pi, pi] in double, its sine and cosine taken in fp32 (absolute error below
- * 4e-7), the rotation done in fp32.  Elements past rope_dim are not rotated.  The 1/sqrt(head_dim) factor stays the attention's `scale` argument.
+ * pos * freqs[i]:  (x, y) -> (x cos - y sin, x sin + y cos).  The angle is formed exactly
+ * (as a sum of two floats) and reduced to [-pi, pi] in fp32 (within 2.3e-7 of the exact
+ * reduced angle for |pos| < 2^24; positions beyond lose that bound), its sine and cosine
+ * taken in fp32 (absolute error below 4e-7), the rotation done in fp32.  Elements past
+ * rope_dim are not rotated.  The 1/sqrt(head_dim) factor stays the attention's `scale`
+ * argument.
  */
 typedef struct {
     const float *freqs;   /* device, [rope_dim / 2]: angular frequency of pair i (pa_rope_yarn_freqs) */

@@ -97,17 +97,25 @@ __device__ __forceinline__ float fast_exp2(float x) {
     return y;
 }
 
-// (cos, sin) of the RoPE angle pos * f: the angle is reduced to about [-pi, pi] in double
-// (one 2 pi constant: the reduced angle is off by under 1e-10 for |pos * f| < 1e6), then
-// __sincosf on the reduced angle (absolute error below 4e-7, far under the bf16 / fp16
-// resolution of the rotated values).
+// (cos, sin) of the RoPE angle pos * f, all in fp32 (fp64 runs at a small fraction of the
+// fp32 rate on this part).  pos * f = hi + lo exactly (two-product: pos < 2^24 is exact
+// in fp32); the angle is reduced by k = rint(hi / 2 pi) turns with 2 pi split in two
+// floats, Cody and Waite's additive reduction: hi - k * C1 is exact (both are multiples of
+// 2^-21 below 8 in magnitude), the small terms -k * C2 + lo take one rounding, the sum one
+// more.  For 0 <= pos < 2^24 the reduced angle is within 2.3e-7 of pos * f mod 2 pi (one
+// fp32 ulp at pi); __sincosf adds under 4e-7 on [-pi, pi].
 __device__ __forceinline__ float2 rope_cos_sin(int pos, float f) {
-    constexpr double kTwoPi = 6.283185307179586476925286766559;
-    constexpr double kInvTwoPi = 0.15915494309189533576888376337251;
-    const double a = (double)pos * (double)f;
-    const double k = rint(a * kInvTwoPi);
+    constexpr float kC1 = 6.28318548202514648f;       // 2 pi rounded to fp32 (0x40c90fdb)
+    constexpr float kC2 = -1.74845553146951720e-7f;   // 2 pi - kC1 rounded to fp32 (0xb43bbd2e)
+    constexpr float kInvTwoPi = 0.159154943091895336f;
+    const float pf = (float)pos;
+    const float hi = pf * f;
+    const float lo = fmaf(pf, f, -hi);
+    const float k = rintf(hi * kInvTwoPi);
+    const float r1 = fmaf(-k, kC1, hi);
+    const float r2 = fmaf(-k, kC2, lo);
     float s, c;
-    __sincosf((float)fma(-k, kTwoPi, a), &s, &c);
+    __sincosf(r1 + r2, &s, &c);
     return make_float2(c, s);
 }
 

@@ -31,6 +31,7 @@ def test_reshape_and_cache_rope_writes_rotated_keys(dtype, rope_dim):
     key = torch.from_numpy(rng.standard_normal((T, Hkv, D)).astype(np.float32)).to(dtype)
     val = torch.from_numpy(rng.standard_normal((T, Hkv, D)).astype(np.float32)).to(dtype)
     pos = rng.integers(0, 200000, size=T).astype(np.int32)
+    pos[[0, 1, 2, 4]] = [(1 << 24) - 1, (1 << 23) + 3, 1 << 20, 0]   # the range the angle bound covers
     slots = rng.permutation(NB * bs)[:T].astype(np.int64)
     slots[[3, 20]] = -1                                   # padding tokens are skipped
     kc = torch.full((NB, bs, Hkv, D), float("nan"), dtype=dtype)
