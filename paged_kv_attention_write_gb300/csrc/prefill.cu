@@ -31,14 +31,17 @@
 //                   over the S row
 //   O  += P_j V_j   tcgen05.mma M128 N=D K128 with A = P from TMEM, fp32 in
 //                   TMEM; V is the MN-major shared-memory operand
-// Warp roles: warps 0 and 6 issue the TMA loads (the Q tile; per key tile one
+// Warp roles: warps 0 and 2 issue the TMA loads (the Q tile; per key tile one
 // 3-D box per block through the block table, issued by the lanes in parallel,
 // into separate K and V rings: a K stage frees when its S finishes, a V stage
-// when its P.V does), warp 1 issues the S products and warp 7 the P.V products
+// when its P.V does), warp 1 issues the S products and warp 3 the P.V products
 // (a thread waits for each MMA to be accepted, so one issuer cannot keep the
-// tensor core busy), warps 2-5 run the softmax and the epilogue.  All
-// shared-memory operands use the 128-byte swizzle.  Every wait is an mbarrier
-// wait bounded in time.
+// tensor core busy), warps 4-11 run the softmax and the epilogue: two threads
+// per query row, one per half of the tile's keys (and of O's columns), which
+// agree on the row's reference max through shared memory once per tile.  All
+// shared-memory operands use the 128-byte swizzle.  Every mbarrier wait is
+// bounded in time; the softmax pairs also exchange a failure flag, so that both
+// threads of a row leave together and no named barrier is left waiting.
 #include <algorithm>
 #include <type_traits>
 
@@ -47,7 +50,7 @@
 namespace pa {
 namespace {
 
-constexpr int kPfThreads = 8 * 32;
+constexpr int kPfThreads = 12 * 32;
 constexpr int kBM = 128;  // query rows per CTA
 constexpr int kBN = 128;  // keys per tile
 constexpr float kRescaleLog2 = 8.f;
@@ -147,6 +150,11 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
     asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
     return r;
 }
+
+// A row's partial max as published to its partner: NaN becomes the canonical NaN, so the
+// pattern kXFail never stands for a score.
+constexpr uint32_t kXFail = 0xFFFFFFFFu;
+__device__ __forceinline__ uint32_t max_bits(float x) { return x != x ? 0x7FC00000u : __float_as_uint(x); }
 
 template <class T>
 __device__ __forceinline__ uint32_t pack2(float lo, float hi);
@@ -333,7 +341,8 @@ struct PfShape {
     static constexpr int OFF_K = OFF_Q + NQ * Q_BYTES;
     static constexpr int OFF_V = OFF_K + NK * KV_BYTES;
     static constexpr int OFF_BAR = OFF_V + NV * KV_BYTES;
-    static constexpr int SMEM = 1024 + OFF_BAR + 512;
+    static constexpr int OFF_X = OFF_BAR + 512;  // row-max / row-sum exchange of the softmax pairs
+    static constexpr int SMEM = 1024 + OFF_X + 1024;
     static_assert(SMEM <= 227 * 1024, "shared memory budget");
     // the unit plan borrows the K ring before the first load
     static_assert((kPlanBins + kPlanBins / 32) * 4 + 2 * kPlanMaxUnits * 2 <= NK * KV_BYTES,
@@ -390,7 +399,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
     // ---- prologue independent of earlier kernels
     if (tid == 0) {
         *abort_flag = 0;
-        for (int i = 0; i < NBAR; ++i) mbar_init(bar(i), (i >= BPF && i < BPF + kSBufs) ? 4 : 1);
+        for (int i = 0; i < NBAR; ++i) mbar_init(bar(i), (i >= BPF && i < BPF + kSBufs) ? 8 : 1);
         fence_barrier_init();
         prefetch_tensormap(&qmap);
         prefetch_tensormap(&kmap);
@@ -420,8 +429,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
     // the Q buffer.
     PfCursor cur;
 
-    if (warp == 0 || warp == 6) {
-        // ============================================ producers (TMA): warp 0 loads Q and K, warp 6 V
+    if (warp == 0 || warp == 2) {
+        // ============================================ producers (TMA): warp 0 loads Q and K, warp 2 V
         // A K stage frees when its S finishes, a V stage when its P.V does, the Q buffer
         // when its item's last S does.  Lane b fetches the block id of the tile's b-th
         // block two tiles ahead and issues that block's boxes; lane 0 posts the tile's
@@ -497,7 +506,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
         if (!ok && lane == 0) *abort_v = 1;
     } else if (warp == 1) {
         // ============================================ S issuer: S_t = Q K_t^T
-        // The S and P.V products are issued by two threads (warps 1 and 7): one thread
+        // The S and P.V products are issued by two threads (warps 1 and 3): one thread
         // waits for each tcgen05.mma to be accepted, so a single issuer keeps the tensor
         // core only about half busy.  S runs up to three tiles ahead of the P.V products;
         // S_t overwrites the P of tile t-3, so it waits until that P.V has finished.
@@ -534,7 +543,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
             }
             if (!ok) *abort_v = 1;
         }
-    } else if (warp == 7) {
+    } else if (warp == 3) {
         // ============================================ P.V issuer: O += P_t V_t, P from TMEM
         if (lane == 0) {
             bool ok = true;
@@ -565,17 +574,32 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
             if (!ok) *abort_v = 1;
         }
     } else {
-        // ============================================ softmax (one thread per query row)
-        const int quarter = warp & 3;            // TMEM lanes this warp may access
-        const int row = quarter * 32 + lane;     // query row of the tile
+        // ============================================ softmax (two threads per query row)
+        // Warps 4-7 take keys 0-63 of every tile and O columns [0, D/2), warps 8-11 keys
+        // 64-127 and O columns [D/2, D).  The two warps on the same TMEM lane quarter form
+        // a pair (named barrier 1 + quarter): once per tile each publishes its rows' partial
+        // max and both take the larger of the two (bit-identical on both sides), so their P
+        // halves share one reference max; a second barrier at the end of the tile keeps the
+        // next tile's publication off the partner's read.  A failed wait is published as
+        // kXFail, and both threads leave at the same point.  Both halves' P is written over
+        // the first 64 columns of the S buffer: the second half's P lands on S columns of
+        // the first half's keys, which that half read before the exchange.
+        const int hh = warp >= 8 ? 1 : 0;
+        const int quarter = warp & 3;                 // TMEM lanes this warp may access
+        const int row = quarter * 32 + lane;          // query row of the tile
+        const int sidx = (warp - 4) * 32 + lane;      // 0..255 over the softmax threads
+        const int pair = 1 + quarter;
+        constexpr int DH = D / 2;
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-        const uint32_t tO = tmem + lane_off + kTmemO;
+        const uint32_t tO = tmem + lane_off + kTmemO + hh * DH;
+        uint32_t *xm = reinterpret_cast<uint32_t *>(smem + Sh::OFF_X);  // [half][row] maxima
+        float *xl = reinterpret_cast<float *>(smem + Sh::OFF_X);        // [half][row] sums, epilogue
         bool ok = true;
         int t = 0;
         cur.fetch(p, 0, planned, my_units);
         for (int k = 0; ok && cur.have; ++k) {
             PfItem it;
-            const bool live = cur.resolve(p, TT, warp == 2 && lane == 0, it);
+            const bool live = cur.resolve(p, TT, warp == 4 && lane == 0, it);
             cur.fetch(p, k + 1, planned, my_units);
             if (!live) continue;
             // rows past the chunk (a ragged last tile) are computed but never stored; they
@@ -583,121 +607,145 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
             const int pos = min(it.pos0 + it.tok_begin + row / G, it.kv_end - 1);
             const int row0_pos = it.pos0 + it.tok_begin;  // position of the tile's first row
             float m_ref = -INFINITY, l = 0.f;
+            bool quit = false;  // the pair saw a failure in the exchange: both leave
             for (int j = 0; j < it.n_tiles; ++j, ++t) {
                 const int sb = t % kSBufs;
-                ok = ok && !*abort_v && mbar_wait(bar(BSF + sb), (t / kSBufs) & 1, p.status);
-                if (!ok) break;
-                tc_fence_after();
+                const bool w_ok = __all_sync(
+                    kFullMask, ok && !*abort_v && mbar_wait(bar(BSF + sb), (t / kSBufs) & 1, p.status));
                 const int k0 = j * kBN;
                 const uint32_t tS = tmem + lane_off + sb * kBN;
-                float sv[kBN];
-                {
-                    uint32_t r0[32], r1[32], r2[32], r3[32];
-                    tmem_ld32(tS, r0);
-                    tmem_ld32(tS + 32, r1);
-                    tmem_ld32(tS + 64, r2);
-                    tmem_ld32(tS + 96, r3);
+                float sv[64];
+                float mloc = -INFINITY;
+                if (w_ok) {
+                    tc_fence_after();
+                    uint32_t r0[32], r1[32];
+                    tmem_ld32(tS + hh * 64, r0);
+                    tmem_ld32(tS + hh * 64 + 32, r1);
                     tmem_wait_ld();
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
                         sv[i] = __uint_as_float(r0[i]);
                         sv[32 + i] = __uint_as_float(r1[i]);
-                        sv[64 + i] = __uint_as_float(r2[i]);
-                        sv[96 + i] = __uint_as_float(r3[i]);
                     }
+                    // mask (keys k0 .. k0+lim-1 are visible; only the last tiles need it) and
+                    // the partial max of the raw scores in eight chains of 3-input maxima
+                    const int lim = min(pos + 1, it.C) - k0 - hh * 64;
+                    if (k0 + kBN > row0_pos + 1 || k0 + kBN > it.C) {  // tile-uniform
+#pragma unroll
+                        for (int c = 0; c < 64; ++c) sv[c] = c < lim ? sv[c] : -INFINITY;
+                    }
+                    float mx8[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) mx8[i] = fmax3(sv[i], sv[8 + i], sv[16 + i]);
+#pragma unroll
+                    for (int c = 24; c + 16 <= 64; c += 16)
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) mx8[i] = fmax3(mx8[i], sv[c + i], sv[c + 8 + i]);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) mx8[i] = fmaxf(mx8[i], sv[56 + i]);
+                    mloc = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
+                                 fmaxf(mx8[6], mx8[7]));
                 }
-                // mask (keys k0 .. k0+lim-1 are visible; only the last tiles need it) and row
-                // max of the raw scores, in eight independent chains of 3-input maxima
-                const int lim = min(pos + 1, it.C) - k0;
-                if (k0 + kBN > row0_pos + 1 || k0 + kBN > it.C) {  // tile-uniform
-#pragma unroll
-                    for (int c = 0; c < kBN; ++c) sv[c] = c < lim ? sv[c] : -INFINITY;
+                xm[hh * kBM + row] = w_ok ? max_bits(mloc) : kXFail;
+                tc_fence_before();
+                named_barrier(pair, 64);
+                tc_fence_after();
+                const uint32_t xa = xm[row], xb = xm[kBM + row];
+                ok = __all_sync(kFullMask, xa != kXFail && xb != kXFail);  // same in both warps
+                if (!ok) {
+                    quit = true;
+                    break;
                 }
-                static_assert(kBN == 128, "max tree layout");
-                float mx8[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) mx8[i] = fmax3(sv[i], sv[8 + i], sv[16 + i]);
-#pragma unroll
-                for (int c = 24; c + 16 <= kBN; c += 16)
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) mx8[i] = fmax3(mx8[i], sv[c + i], sv[c + 8 + i]);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) mx8[i] = fmaxf(mx8[i], sv[120 + i]);
-                const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
-                                       fmaxf(mx8[6], mx8[7])) *
-                                 p.qk_scale_log2;
+                const float mx = fmaxf(__uint_as_float(xa), __uint_as_float(xb)) * p.qk_scale_log2;
                 // lazy rescale; warp-uniform because the O row is read and written by the
-                // whole warp (tcgen05.ld / st)
+                // whole warp (tcgen05.ld / st), and the same in both warps of the pair
                 const bool grow = mx > m_ref + kRescaleLog2;
                 if (__any_sync(kFullMask, grow)) {
                     const float m_new = grow ? mx : m_ref;
                     const float alpha = m_new == m_ref ? 1.f : fast_exp2(m_ref - m_new);  // 0 from -inf
                     l *= alpha;
                     m_ref = m_new;
-                    if (j >= 1) {  // O holds tiles < j: wait for the last P.V, then scale the row
-                        ok = ok && mbar_wait(bar(BPV + (t - 1) % kSBufs), ((t - 1) / kSBufs) & 1, p.status);
-                        tc_fence_after();
+                    if (j >= 1) {  // O holds tiles < j: wait for the last P.V, then scale my columns
+                        ok = __all_sync(kFullMask, mbar_wait(bar(BPV + (t - 1) % kSBufs), ((t - 1) / kSBufs) & 1,
+                                                             p.status));
+                        if (ok) {
+                            tc_fence_after();
 #pragma unroll
-                        for (int c0 = 0; c0 < D; c0 += 32) {
-                            uint32_t r[32];
-                            tmem_ld32(tO + c0, r);
-                            tmem_wait_ld();
+                            for (int c0 = 0; c0 < DH; c0 += 32) {
+                                uint32_t r[32];
+                                tmem_ld32(tO + c0, r);
+                                tmem_wait_ld();
 #pragma unroll
-                            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-                            tmem_st32(tO + c0, r);
+                                for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+                                tmem_st32(tO + c0, r);
+                            }
+                            tmem_wait_st();
                         }
-                        tmem_wait_st();
                     }
                 }
-                // P row over the S row just read: 128 keys packed two per TMEM column (the
-                // P.V of this buffer's previous tile finished before this S was issued)
-                const float2 sc2 = make_float2(p.qk_scale_log2, p.qk_scale_log2), nm2 = make_float2(-m_ref, -m_ref);
-                float2 rs2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
+                // my 64 weights, packed two per TMEM column (the P.V of this buffer's previous
+                // tile finished before this S was issued)
+                {
+                    const float2 sc2 = make_float2(p.qk_scale_log2, p.qk_scale_log2), nm2 = make_float2(-m_ref, -m_ref);
+                    float2 rs2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
                     uint32_t w[32];
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
-                        const int c = half * 64 + 2 * i;
-                        const float2 x = __ffma2_rn(make_float2(sv[c], sv[c + 1]), sc2, nm2);
+                        const float2 x = __ffma2_rn(make_float2(sv[2 * i], sv[2 * i + 1]), sc2, nm2);
                         w[i] = pack2<T>(fast_exp2(x.x), fast_exp2(x.y));
                         rs2[i & 1] = __fadd2_rn(rs2[i & 1], unpack2<T>(w[i]));
                     }
-                    tmem_st32(tS + half * 32, w);
+                    if (ok) {
+                        tmem_st32(tS + hh * 32, w);
+                        tmem_wait_st();
+                    }
+                    l += (rs2[0].x + rs2[0].y) + (rs2[1].x + rs2[1].y);
                 }
-                tmem_wait_st();
-                l += (rs2[0].x + rs2[0].y) + (rs2[1].x + rs2[1].y);
                 // keys past kv_end in this tile (not loaded, or past the context): zero V rows,
                 // so that 0-weight rows never meet stale or NaN data
                 if (k0 + kBN > it.kv_end) {
                     const int valid = it.kv_end - k0, st = t % NV;
                     ok = ok && mbar_wait(bar(BVF + st), (t / NV) & 1, p.status);
                     const uint32_t sV = sV0 + st * Sh::KV_BYTES;
-                    for (int i = tid - 64; i < (kBN - valid) * Sh::HALVES * 8; i += 128) {
-                        const int rr = valid + i / (Sh::HALVES * 8), rest = i % (Sh::HALVES * 8);
-                        sts128(sV + (rest / 8) * (kBN * 128) + rr * 128 + (rest % 8) * 16, 0u, 0u, 0u, 0u);
-                    }
+                    if (ok)
+                        for (int i = sidx; i < (kBN - valid) * Sh::HALVES * 8; i += 256) {
+                            const int rr = valid + i / (Sh::HALVES * 8), rest = i % (Sh::HALVES * 8);
+                            sts128(sV + (rest / 8) * (kBN * 128) + rr * 128 + (rest % 8) * 16, 0u, 0u, 0u, 0u);
+                        }
                     fence_async_smem();
                 }
+                named_barrier(pair, 64);  // both have read this tile's maxima
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(BPF + sb));
             }
-            if (!ok) break;
+            if (quit) break;  // together with the partner; a later local failure goes
+                              // through the epilogue's exchange
             // ---- epilogue: O / l for the rows of this chunk.  The next item's first P.V
-            // (which overwrites O) waits for P written later by these same threads.
+            // (which overwrites O) waits for P written later by these same threads.  The
+            // pair adds its two partial row sums (and exchanges the failure flag) through
+            // the exchange area (the last tile's maxima have been read by both): a barrier
+            // after the sums are written and one after they are read.
             const int last = t - 1;
-            ok = mbar_wait(bar(BPV + last % kSBufs), (last / kSBufs) & 1, p.status);
+            const bool e_ok = __all_sync(kFullMask, ok && mbar_wait(bar(BPV + last % kSBufs), (last / kSBufs) & 1,
+                                                                    p.status));
+            xl[hh * kBM + row] = e_ok ? l : -1.f;  // row sums are >= 0 (or NaN): -1 flags a failure
+            named_barrier(pair, 64);
+            const float la = xl[row], lb = xl[kBM + row];
+            named_barrier(pair, 64);
+            ok = __all_sync(kFullMask, la != -1.f && lb != -1.f);
+            if (!ok) break;
             tc_fence_after();
             const int tok = it.tok_begin + row / G;
-            const float inv = l > 0.f ? 1.f / l : 0.f;
-            const int64_t orow = ((int64_t)(it.q0 + tok) * Hq + it.g * G + row % G) * D;
+            const float lsum = la + lb;
+            const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+            const int64_t orow = ((int64_t)(it.q0 + tok) * Hq + it.g * G + row % G) * D + hh * DH;
 #pragma unroll
-            for (int c0 = 0; c0 < D; c0 += 32) {
+            for (int c0 = 0; c0 < DH; c0 += 32) {
                 uint32_t r[32];
                 tmem_ld32(tO + c0, r);
                 tmem_wait_ld();
-                if (ok && tok < it.Lq) {
+                if (tok < it.Lq) {
                     if (p.out_dtype == PA_F32) {
                         float4 *o = reinterpret_cast<float4 *>(static_cast<float *>(p.out) + orow + c0);
 #pragma unroll
