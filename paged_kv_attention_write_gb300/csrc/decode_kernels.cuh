@@ -392,6 +392,13 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
         prefetch_tensormap(&kmap);
         prefetch_tensormap(&vmap);
     }
+    if (warp == NW) {  // the block tables (spread over the CTAs) and the context lengths into L2
+        const int64_t bt_lines = ((int64_t)p.num_seqs * p.max_blocks_per_seq * 4 + 127) / 128;
+        const int lines = bt_lines < (1 << 30) ? (int)bt_lines : (1 << 30);
+        for (int i = blockIdx.x * 32 + lane; i < lines; i += gridDim.x * 32)
+            prefetch_l2(reinterpret_cast<const char *>(p.block_tables) + (int64_t)i * 128);
+        if (lane * 32 < p.num_seqs) prefetch_l2(p.context_lens + lane * 32);
+    }
     pdl_wait_previous();      // context lengths, block tables, caches (and the plan) are ready
     pdl_launch_dependents();  // the reduce kernel may launch; it waits for our completion
 
@@ -747,12 +754,12 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
 // ------------------------------------------------------------------------------ reduce kernel
 
 constexpr int kMaxPieces = 1024;  // CTAs of the split kernel (one per SM)
-constexpr int kReduceBatch = 16;  // pieces whose loads are in flight together
+constexpr int kReduceBatch = 32;  // pieces whose loads are in flight together
 
 // For every segment split over several CTAs: out = sum_c 2^(m_c - M) acc_c /
 // sum_c 2^(m_c - M) l_c.  grid = (segment, query head of the group); one thread
 // per pair of outputs.  The loads of a batch of pieces are all issued before any
-// is used (two memory round trips for the usual segment of < 16 pieces), and the
+// is used (two memory round trips for the usual segment of < 32 pieces), and the
 // batch is merged online (running max).
 template <int D>
 __global__ void __launch_bounds__(D / 2) decode_reduce_kernel(const DecodeParams p, int HGq) {
