@@ -131,6 +131,32 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
         "r"(r[29]), "r"(r[30]), "r"(r[31])
         : "memory");
 }
+// 16 lanes x N groups of 8 consecutive 32-bit columns -> 4N registers per thread: thread t
+// holds rows t/4 and t/4 + 8 of the 16, columns 8j + 2(t%4) and the next one of group j, as
+// registers 4j, 4j+1 (first row) and 4j+2, 4j+3 (second row).
+template <int N>
+__device__ __forceinline__ void tmem_ld_16x256b(uint32_t taddr, uint32_t (&r)[4 * N]);
+template <>
+__device__ __forceinline__ void tmem_ld_16x256b<4>(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x256b.x4.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+template <>
+__device__ __forceinline__ void tmem_ld_16x256b<8>(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x256b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+          "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+          "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+}
+
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
@@ -404,6 +430,16 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
         prefetch_tensormap(&qmap);
         prefetch_tensormap(&kmap);
         prefetch_tensormap(&vmap);
+    }
+    if (warp == 2) {  // the block tables (spread over the CTAs), query offsets and context lengths into L2
+        const int64_t bt_lines = ((int64_t)p.num_seqs * p.max_blocks_per_seq * 4 + 127) / 128;
+        const int lines = bt_lines < (1 << 30) ? (int)bt_lines : (1 << 30);
+        for (int i = blockIdx.x * 32 + lane; i < lines; i += gridDim.x * 32)
+            prefetch_l2(reinterpret_cast<const char *>(p.block_tables) + (int64_t)i * 128);
+        if (lane * 32 <= p.num_seqs) {
+            prefetch_l2(p.query_start_loc + lane * 32);
+            if (lane * 32 < p.num_seqs) prefetch_l2(p.context_lens + lane * 32);
+        }
     }
     pdl_wait_previous();
     pdl_launch_dependents();
@@ -739,20 +775,49 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
             const int tok = it.tok_begin + row / G;
             const float lsum = la + lb;
             const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-            const int64_t orow = ((int64_t)(it.q0 + tok) * Hq + it.g * G + row % G) * D + hh * DH;
+            if (p.out_dtype == PA_F32) {
+                // fp32 rows through the 16-lane TMEM shape: lanes 4i..4i+3 hold two rows, two
+                // columns each per group of 8; one swap with the neighbouring lane gives each
+                // lane four consecutive columns, so a store instruction writes 64 contiguous
+                // bytes of each of 8 rows (one row per lane would touch 32 lines)
+                float *outf = static_cast<float *>(p.out);
+                const int gi = lane >> 2, ga = lane & 3;
+                const bool odd = (ga & 1) != 0;
 #pragma unroll
-            for (int c0 = 0; c0 < DH; c0 += 32) {
-                uint32_t r[32];
-                tmem_ld32(tO + c0, r);
-                tmem_wait_ld();
-                if (tok < it.Lq) {
-                    if (p.out_dtype == PA_F32) {
-                        float4 *o = reinterpret_cast<float4 *>(static_cast<float *>(p.out) + orow + c0);
+                for (int slab = 0; slab < 2; ++slab) {
+                    uint32_t r[DH / 2];
+                    tmem_ld_16x256b<DH / 8>(tmem + ((uint32_t)(quarter * 32 + slab * 16) << 16) + kTmemO + hh * DH, r);
+                    tmem_wait_ld();
 #pragma unroll
-                        for (int i = 0; i < 8; ++i)
-                            o[i] = make_float4(__uint_as_float(r[4 * i]) * inv, __uint_as_float(r[4 * i + 1]) * inv,
-                                               __uint_as_float(r[4 * i + 2]) * inv, __uint_as_float(r[4 * i + 3]) * inv);
-                    } else {
+                    for (int rh = 0; rh < 2; ++rh) {  // rows slab*16 + gi and slab*16 + 8 + gi of the quarter
+                        const int qrow = slab * 16 + rh * 8 + gi, trow = quarter * 32 + qrow;
+                        const float rinv = __shfl_sync(kFullMask, inv, qrow);
+                        const int rtok = it.tok_begin + trow / G;
+                        float *orow_p = outf + ((int64_t)(it.q0 + rtok) * Hq + it.g * G + trow % G) * D + hh * DH;
+#pragma unroll
+                        for (int j = 0; j < DH / 8; j += 2) {
+                            const int e0 = 4 * j + 2 * rh, e1 = 4 * (j + 1) + 2 * rh;  // this row's pair in groups j, j+1
+                            const float2 keep = odd ? make_float2(__uint_as_float(r[e1]), __uint_as_float(r[e1 + 1]))
+                                                    : make_float2(__uint_as_float(r[e0]), __uint_as_float(r[e0 + 1]));
+                            const float2 send = odd ? make_float2(__uint_as_float(r[e0]), __uint_as_float(r[e0 + 1]))
+                                                    : make_float2(__uint_as_float(r[e1]), __uint_as_float(r[e1 + 1]));
+                            const float2 got = make_float2(__shfl_xor_sync(kFullMask, send.x, 1),
+                                                           __shfl_xor_sync(kFullMask, send.y, 1));
+                            const int col = odd ? 8 * (j + 1) + 2 * (ga - 1) : 8 * j + 2 * ga;
+                            const float4 v = odd ? make_float4(got.x * rinv, got.y * rinv, keep.x * rinv, keep.y * rinv)
+                                                 : make_float4(keep.x * rinv, keep.y * rinv, got.x * rinv, got.y * rinv);
+                            if (rtok < it.Lq) *reinterpret_cast<float4 *>(orow_p + col) = v;
+                        }
+                    }
+                }
+            } else {
+                const int64_t orow = ((int64_t)(it.q0 + tok) * Hq + it.g * G + row % G) * D + hh * DH;
+#pragma unroll
+                for (int c0 = 0; c0 < DH; c0 += 32) {
+                    uint32_t r[32];
+                    tmem_ld32(tO + c0, r);
+                    tmem_wait_ld();
+                    if (tok < it.Lq) {
 #pragma unroll
                         for (int i = 0; i < 16; ++i) {
                             const float a = __uint_as_float(r[2 * i]) * inv, b = __uint_as_float(r[2 * i + 1]) * inv;
