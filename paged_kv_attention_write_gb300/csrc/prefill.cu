@@ -772,62 +772,64 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
             ok = __all_sync(kFullMask, la != -1.f && lb != -1.f);
             if (!ok) break;
             tc_fence_after();
-            const int tok = it.tok_begin + row / G;
             const float lsum = la + lb;
             const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-            if (p.out_dtype == PA_F32) {
-                // fp32 rows through the 16-lane TMEM shape: lanes 4i..4i+3 hold two rows, two
-                // columns each per group of 8; one swap with the neighbouring lane gives each
-                // lane four consecutive columns, so a store instruction writes 64 contiguous
-                // bytes of each of 8 rows (one row per lane would touch 32 lines)
-                float *outf = static_cast<float *>(p.out);
+            {
+                // Output rows through the 16-lane TMEM shape: lanes 4i..4i+3 hold two rows,
+                // two columns each per group of 8; one swap with the neighbouring lane gives
+                // each lane four consecutive columns, so a store instruction writes 64 (fp32)
+                // or 32 (fp16 / bf16) contiguous bytes of each of 8 rows, where one row per
+                // lane would touch 32 lines
                 const int gi = lane >> 2, ga = lane & 3;
                 const bool odd = (ga & 1) != 0;
+                auto write_rows = [&](auto out_tag) {  // one copy of the loops per output type
+                    using OT = decltype(out_tag);
+                    OT *outp = static_cast<OT *>(p.out);
 #pragma unroll
-                for (int slab = 0; slab < 2; ++slab) {
-                    uint32_t r[DH / 2];
-                    tmem_ld_16x256b<DH / 8>(tmem + ((uint32_t)(quarter * 32 + slab * 16) << 16) + kTmemO + hh * DH, r);
-                    tmem_wait_ld();
+                    for (int slab = 0; slab < 2; ++slab) {
+                        uint32_t r[DH / 2];
+                        tmem_ld_16x256b<DH / 8>(tmem + ((uint32_t)(quarter * 32 + slab * 16) << 16) + kTmemO + hh * DH, r);
+                        tmem_wait_ld();
 #pragma unroll
-                    for (int rh = 0; rh < 2; ++rh) {  // rows slab*16 + gi and slab*16 + 8 + gi of the quarter
-                        const int qrow = slab * 16 + rh * 8 + gi, trow = quarter * 32 + qrow;
-                        const float rinv = __shfl_sync(kFullMask, inv, qrow);
-                        const int rtok = it.tok_begin + trow / G;
-                        float *orow_p = outf + ((int64_t)(it.q0 + rtok) * Hq + it.g * G + trow % G) * D + hh * DH;
+                        for (int rh = 0; rh < 2; ++rh) {  // rows slab*16 + gi and slab*16 + 8 + gi of the quarter
+                            const int qrow = slab * 16 + rh * 8 + gi, trow = quarter * 32 + qrow;
+                            const float rinv = __shfl_sync(kFullMask, inv, qrow);
+                            const int rtok = it.tok_begin + trow / G;
+                            const int64_t obase = ((int64_t)(it.q0 + rtok) * Hq + it.g * G + trow % G) * D + hh * DH;
 #pragma unroll
-                        for (int j = 0; j < DH / 8; j += 2) {
-                            const int e0 = 4 * j + 2 * rh, e1 = 4 * (j + 1) + 2 * rh;  // this row's pair in groups j, j+1
-                            const float2 keep = odd ? make_float2(__uint_as_float(r[e1]), __uint_as_float(r[e1 + 1]))
-                                                    : make_float2(__uint_as_float(r[e0]), __uint_as_float(r[e0 + 1]));
-                            const float2 send = odd ? make_float2(__uint_as_float(r[e0]), __uint_as_float(r[e0 + 1]))
-                                                    : make_float2(__uint_as_float(r[e1]), __uint_as_float(r[e1 + 1]));
-                            const float2 got = make_float2(__shfl_xor_sync(kFullMask, send.x, 1),
-                                                           __shfl_xor_sync(kFullMask, send.y, 1));
-                            const int col = odd ? 8 * (j + 1) + 2 * (ga - 1) : 8 * j + 2 * ga;
-                            const float4 v = odd ? make_float4(got.x * rinv, got.y * rinv, keep.x * rinv, keep.y * rinv)
-                                                 : make_float4(keep.x * rinv, keep.y * rinv, got.x * rinv, got.y * rinv);
-                            if (rtok < it.Lq) *reinterpret_cast<float4 *>(orow_p + col) = v;
+                            for (int j = 0; j < DH / 8; j += 2) {
+                                const int e0 = 4 * j + 2 * rh, e1 = 4 * (j + 1) + 2 * rh;  // this row's pair in groups j, j+1
+                                const float2 keep = odd ? make_float2(__uint_as_float(r[e1]), __uint_as_float(r[e1 + 1]))
+                                                        : make_float2(__uint_as_float(r[e0]), __uint_as_float(r[e0 + 1]));
+                                const float2 send = odd ? make_float2(__uint_as_float(r[e0]), __uint_as_float(r[e0 + 1]))
+                                                        : make_float2(__uint_as_float(r[e1]), __uint_as_float(r[e1 + 1]));
+                                const float2 got = make_float2(__shfl_xor_sync(kFullMask, send.x, 1),
+                                                               __shfl_xor_sync(kFullMask, send.y, 1));
+                                const int col = odd ? 8 * (j + 1) + 2 * (ga - 1) : 8 * j + 2 * ga;
+                                const float4 v = odd ? make_float4(got.x * rinv, got.y * rinv, keep.x * rinv, keep.y * rinv)
+                                                     : make_float4(keep.x * rinv, keep.y * rinv, got.x * rinv, got.y * rinv);
+                                if (rtok >= it.Lq) continue;
+                                if constexpr (std::is_same<OT, float>::value) {
+                                    *reinterpret_cast<float4 *>(outp + obase + col) = v;
+                                } else if constexpr (std::is_same<OT, __half>::value) {
+                                    __half2 lo = __floats2half2_rn(v.x, v.y), hi = __floats2half2_rn(v.z, v.w);
+                                    *reinterpret_cast<uint2 *>(outp + obase + col) =
+                                        make_uint2(*reinterpret_cast<uint32_t *>(&lo), *reinterpret_cast<uint32_t *>(&hi));
+                                } else {
+                                    __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
+                                    *reinterpret_cast<uint2 *>(outp + obase + col) =
+                                        make_uint2(*reinterpret_cast<uint32_t *>(&lo), *reinterpret_cast<uint32_t *>(&hi));
+                                }
+                            }
                         }
                     }
-                }
-            } else {
-                const int64_t orow = ((int64_t)(it.q0 + tok) * Hq + it.g * G + row % G) * D + hh * DH;
-#pragma unroll
-                for (int c0 = 0; c0 < DH; c0 += 32) {
-                    uint32_t r[32];
-                    tmem_ld32(tO + c0, r);
-                    tmem_wait_ld();
-                    if (tok < it.Lq) {
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            const float a = __uint_as_float(r[2 * i]) * inv, b = __uint_as_float(r[2 * i + 1]) * inv;
-                            if (p.out_dtype == PA_F16)
-                                store_out(static_cast<__half *>(p.out) + orow + c0 + 2 * i, a, b);
-                            else
-                                store_out(static_cast<__nv_bfloat16 *>(p.out) + orow + c0 + 2 * i, a, b);
-                        }
-                    }
-                }
+                };
+                if (p.out_dtype == PA_F32)
+                    write_rows(float{});
+                else if (p.out_dtype == PA_F16)
+                    write_rows(__half{});
+                else
+                    write_rows(__nv_bfloat16{});
             }
             tc_fence_before();
         }
