@@ -32,16 +32,14 @@
 //   O  += P_j V_j   tcgen05.mma M128 N=D K128 with A = P from TMEM, fp32 in
 //                   TMEM; V is the MN-major shared-memory operand
 // Warp roles: warps 0 and 2 issue the TMA loads (the Q tile; per key tile one
-// 3-D box per block through the block table, issued by the lanes in parallel,
+// 5-D box per block through the block table, issued by the lanes in parallel,
 // into separate K and V rings: a K stage frees when its S finishes, a V stage
 // when its P.V does), warp 1 issues the S products and warp 3 the P.V products
 // (a thread waits for each MMA to be accepted, so one issuer cannot keep the
-// tensor core busy), warps 4-11 run the softmax and the epilogue: two threads
-// per query row, one per half of the tile's keys (and of O's columns), which
-// agree on the row's reference max through shared memory once per tile.  All
-// shared-memory operands use the 128-byte swizzle.  Every mbarrier wait is
-// bounded in time; the softmax pairs also exchange a failure flag, so that both
-// threads of a row leave together and no named barrier is left waiting.
+// tensor core busy), warps 4-11 run the softmax and the epilogue, two warps per
+// TMEM lane quarter, each on a 16-row slab through the 16-lane TMEM shapes (a row's
+// keys spread over four lanes).  All shared-memory operands use the 128-byte swizzle.
+// Every mbarrier wait is bounded in time.
 #include <algorithm>
 #include <type_traits>
 
@@ -108,42 +106,11 @@ __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// 32 lanes x 32 consecutive 32-bit TMEM columns <-> 32 registers per thread.
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
-          "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
-          "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-        : "r"(taddr));
-}
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
-        "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
-        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
-        "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
-        "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
-        "r"(r[29]), "r"(r[30]), "r"(r[31])
-        : "memory");
-}
 // 16 lanes x N groups of 8 consecutive 32-bit columns -> 4N registers per thread: thread t
 // holds rows t/4 and t/4 + 8 of the 16, columns 8j + 2(t%4) and the next one of group j, as
 // registers 4j, 4j+1 (first row) and 4j+2, 4j+3 (second row).
 template <int N>
 __device__ __forceinline__ void tmem_ld_16x256b(uint32_t taddr, uint32_t (&r)[4 * N]);
-template <>
-__device__ __forceinline__ void tmem_ld_16x256b<4>(uint32_t taddr, uint32_t (&r)[16]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.16x256b.x4.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr));
-}
 template <>
 __device__ __forceinline__ void tmem_ld_16x256b<8>(uint32_t taddr, uint32_t (&r)[32]) {
     asm volatile(
@@ -155,6 +122,29 @@ __device__ __forceinline__ void tmem_ld_16x256b<8>(uint32_t taddr, uint32_t (&r)
           "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
           "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
         : "r"(taddr));
+}
+
+// The 16-lane shapes in the other direction: 16x256b as loaded above, and 16x128b, where
+// thread t holds column 4j + t%4 of rows t/4 and t/4 + 8 of group j (registers 2j, 2j+1).
+__device__ __forceinline__ void tmem_st_16x256b_x8(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.16x256b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
+        "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
+        "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+__device__ __forceinline__ void tmem_st_16x128b_x16(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.16x128b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
+        "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
+        "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
 }
 
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
@@ -176,11 +166,6 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
     asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
     return r;
 }
-
-// A row's partial max as published to its partner: NaN becomes the canonical NaN, so the
-// pattern kXFail never stands for a score.
-constexpr uint32_t kXFail = 0xFFFFFFFFu;
-__device__ __forceinline__ uint32_t max_bits(float x) { return x != x ? 0x7FC00000u : __float_as_uint(x); }
 
 template <class T>
 __device__ __forceinline__ uint32_t pack2(float lo, float hi);
@@ -359,7 +344,8 @@ template <int D>
 struct PfShape {
     static constexpr int HALVES = D / 64;             // 128-byte swizzle atoms along D
     static constexpr int Q_BYTES = kBM * D * 2;       // [half][128 rows][128 B]
-    static constexpr int KV_BYTES = kBN * D * 2;      // one K (or V) stage, same layout
+    static constexpr int KV_BYTES = kBN * D * 2;      // one K (or V) stage: [8-key group][slice][8 keys][128 B]
+    static constexpr int GSTR = HALVES * 1024;        // bytes between 8-key groups of a K / V stage
     static constexpr int NQ = D == 64 ? 2 : 1;        // Q buffers
     static constexpr int NK = D == 64 ? 4 : 3;        // K stages
     static constexpr int NV = D == 64 ? 4 : 3;        // V stages
@@ -367,8 +353,7 @@ struct PfShape {
     static constexpr int OFF_K = OFF_Q + NQ * Q_BYTES;
     static constexpr int OFF_V = OFF_K + NK * KV_BYTES;
     static constexpr int OFF_BAR = OFF_V + NV * KV_BYTES;
-    static constexpr int OFF_X = OFF_BAR + 512;  // row-max / row-sum exchange of the softmax pairs
-    static constexpr int SMEM = 1024 + OFF_X + 1024;
+    static constexpr int SMEM = 1024 + OFF_BAR + 512;
     static_assert(SMEM <= 227 * 1024, "shared memory budget");
     // the unit plan borrows the K ring before the first load
     static_assert((kPlanBins + kPlanBins / 32) * 4 + 2 * kPlanMaxUnits * 2 <= NK * KV_BYTES,
@@ -478,7 +463,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
         const int bar_full = is_k ? BKF : BVF, bar_empty = is_k ? BKE : BVE;
         const uint64_t policy = policy_evict_first();
         const int nb = kBN / bs;  // blocks per key tile (4, 8 or 16)
-        const uint32_t box_bytes = (uint32_t)bs * 128;  // one block of one kv head, one D half
+        const uint32_t box_bytes = (uint32_t)bs * 128 * Sh::HALVES;  // one block of one kv head
         bool ok = true;
         int t = 0, vi = 0;
         cur.fetch(p, 0, planned, my_units);
@@ -527,12 +512,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
                 const bool valid = in_range && my_id >= 0 && my_id < p.num_blocks;
                 if (in_range && !valid) report(p.status, PA_DEVERR_BLOCK_ID);  // never dereferenced
                 const unsigned mine = __ballot_sync(kFullMask, valid);
-                if (lane == 0) mbar_expect_tx(full, __popc(mine) * Sh::HALVES * box_bytes);
+                if (lane == 0) mbar_expect_tx(full, __popc(mine) * box_bytes);
                 __syncwarp();
                 if (valid) {
                     const uint32_t dst = ring + st * Sh::KV_BYTES + lane * box_bytes;
-                    for (int hf = 0; hf < Sh::HALVES; ++hf)
-                        tma_load_3d(dst + hf * (kBN * 128), map, hf * 64, it.g, my_id * bs, full, policy);
+                    tma_load_5d(dst, map, 0, 0, 0, my_id * (bs / 8), it.g, full, policy);
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(full);
@@ -568,7 +552,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
 #pragma unroll
                     for (int ks = 0; ks < KSTEPS_S; ++ks) {
                         const uint32_t off = (ks / 4) * (kBM * 128) + (ks % 4) * 32;
-                        mma_f16(tmem + sb * kBN, smem_desc(sQ + off, 16, 1024), smem_desc(sK + off, 16, 1024),
+                        const uint32_t offk = (ks / 4) * 1024 + (ks % 4) * 32;
+                        mma_f16(tmem + sb * kBN, smem_desc(sQ + off, 16, 1024), smem_desc(sK + offk, 16, Sh::GSTR),
                                 IDESC_S, ks > 0 ? 1u : 0u);
                     }
                     mma_commit(bar(BSF + sb));
@@ -599,7 +584,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
                     const uint32_t sV = sV0 + st * Sh::KV_BYTES;
 #pragma unroll
                     for (int kk = 0; kk < KSTEPS_PV; ++kk) {
-                        const uint64_t db = smem_desc(sV + kk * 16 * 128, kBN * 128, 1024);
+                        const uint64_t db = smem_desc(sV + kk * 2 * Sh::GSTR, 1024, Sh::GSTR);
                         mma_f16_tmem_a(tmem + kTmemO, tmem + pb * kBN + kk * 8, db, IDESC_PV,
                                        (j > 0 || kk > 0) ? 1u : 0u);
                     }
@@ -610,26 +595,23 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
             if (!ok) *abort_v = 1;
         }
     } else {
-        // ============================================ softmax (two threads per query row)
-        // Warps 4-7 take keys 0-63 of every tile and O columns [0, D/2), warps 8-11 keys
-        // 64-127 and O columns [D/2, D).  The two warps on the same TMEM lane quarter form
-        // a pair (named barrier 1 + quarter): once per tile each publishes its rows' partial
-        // max and both take the larger of the two (bit-identical on both sides), so their P
-        // halves share one reference max; a second barrier at the end of the tile keeps the
-        // next tile's publication off the partner's read.  A failed wait is published as
-        // kXFail, and both threads leave at the same point.  Both halves' P is written over
-        // the first 64 columns of the S buffer: the second half's P lands on S columns of
-        // the first half's keys, which that half read before the exchange.
-        const int hh = warp >= 8 ? 1 : 0;
-        const int quarter = warp & 3;                 // TMEM lanes this warp may access
-        const int row = quarter * 32 + lane;          // query row of the tile
+        // ============================================ softmax (row slabs)
+        // Warps 4-7 take rows 0-15 and warps 8-11 rows 16-31 of the TMEM lane quarter
+        // warp % 4, through the 16-lane TMEM shapes: in 16x256b a thread holds rows t/4 and
+        // t/4 + 8 of its slab, keys 8j + 2(t%4) and the next one of each group of 8, so a row
+        // is spread over the four lanes 4(t/4) .. 4(t/4)+3 (row maxima and sums are two
+        // shuffles among them) and the pair of keys a thread holds packs into the P column
+        // 4j + t%4, exactly the 16x128b store layout.  The two warps of a quarter share no
+        // state, so each hides the other's latencies.
+        const int quarter = warp & 3;
+        const int slab = warp >= 8 ? 1 : 0;
+        const int gi = lane >> 2, ga = lane & 3;
         const int sidx = (warp - 4) * 32 + lane;      // 0..255 over the softmax threads
-        const int pair = 1 + quarter;
-        constexpr int DH = D / 2;
-        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-        const uint32_t tO = tmem + lane_off + kTmemO + hh * DH;
-        uint32_t *xm = reinterpret_cast<uint32_t *>(smem + Sh::OFF_X);  // [half][row] maxima
-        float *xl = reinterpret_cast<float *>(smem + Sh::OFF_X);        // [half][row] sums, epilogue
+        const int lane0 = quarter * 32 + slab * 16;   // first TMEM lane (tile row) of the slab
+        const int row0 = lane0 + gi, row1 = row0 + 8; // this thread's two rows of the tile
+        const uint32_t lane_off = (uint32_t)lane0 << 16;
+        const uint32_t tO = tmem + lane_off + kTmemO;
+        const float sc = p.qk_scale_log2;
         bool ok = true;
         int t = 0;
         cur.fetch(p, 0, planned, my_units);
@@ -640,197 +622,200 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
             if (!live) continue;
             // rows past the chunk (a ragged last tile) are computed but never stored; they
             // see exactly the keys that were loaded
-            const int pos = min(it.pos0 + it.tok_begin + row / G, it.kv_end - 1);
+            const int pos0 = min(it.pos0 + it.tok_begin + row0 / G, it.kv_end - 1);
+            const int pos1 = min(it.pos0 + it.tok_begin + row1 / G, it.kv_end - 1);
             const int row0_pos = it.pos0 + it.tok_begin;  // position of the tile's first row
-            float m_ref = -INFINITY, l = 0.f;
-            bool quit = false;  // the pair saw a failure in the exchange: both leave
+            float m0 = -INFINITY, m1 = -INFINITY;        // reference maxima (log2 domain)
+            float l0 = 0.f, l1 = 0.f;                     // this lane's share of the row sums
             for (int j = 0; j < it.n_tiles; ++j, ++t) {
                 const int sb = t % kSBufs;
-                const bool w_ok = __all_sync(
-                    kFullMask, ok && !*abort_v && mbar_wait(bar(BSF + sb), (t / kSBufs) & 1, p.status));
+                ok = __all_sync(kFullMask, ok && !*abort_v && mbar_wait(bar(BSF + sb), (t / kSBufs) & 1, p.status));
+                if (!ok) break;
+                tc_fence_after();
                 const int k0 = j * kBN;
                 const uint32_t tS = tmem + lane_off + sb * kBN;
-                float sv[64];
-                float mloc = -INFINITY;
-                if (w_ok) {
-                    tc_fence_after();
-                    uint32_t r0[32], r1[32];
-                    tmem_ld32(tS + hh * 64, r0);
-                    tmem_ld32(tS + hh * 64 + 32, r1);
-                    tmem_wait_ld();
+                uint32_t s[2][32];  // keys 0-63 and 64-127 of the tile
+                tmem_ld_16x256b<8>(tS, s[0]);
+                tmem_ld_16x256b<8>(tS + 64, s[1]);
+                tmem_wait_ld();
+                // mask (keys k0 .. k0+lim-1 are visible to a row; only the last tiles need it)
+                if (k0 + kBN > row0_pos + 1 || k0 + kBN > it.C) {  // tile-uniform
+                    const int lim0 = min(pos0 + 1, it.C) - k0, lim1 = min(pos1 + 1, it.C) - k0;
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        sv[i] = __uint_as_float(r0[i]);
-                        sv[32 + i] = __uint_as_float(r1[i]);
-                    }
-                    // mask (keys k0 .. k0+lim-1 are visible; only the last tiles need it) and
-                    // the partial max of the raw scores in eight chains of 3-input maxima
-                    const int lim = min(pos + 1, it.C) - k0 - hh * 64;
-                    if (k0 + kBN > row0_pos + 1 || k0 + kBN > it.C) {  // tile-uniform
+                    for (int h = 0; h < 2; ++h)
 #pragma unroll
-                        for (int c = 0; c < 64; ++c) sv[c] = c < lim ? sv[c] : -INFINITY;
-                    }
-                    float mx8[8];
+                        for (int g = 0; g < 8; ++g)
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) mx8[i] = fmax3(sv[i], sv[8 + i], sv[16 + i]);
-#pragma unroll
-                    for (int c = 24; c + 16 <= 64; c += 16)
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) mx8[i] = fmax3(mx8[i], sv[c + i], sv[c + 8 + i]);
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) mx8[i] = fmaxf(mx8[i], sv[56 + i]);
-                    mloc = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
-                                 fmaxf(mx8[6], mx8[7]));
+                            for (int e = 0; e < 2; ++e) {
+                                const int key = h * 64 + 8 * g + 2 * ga + e;
+                                if (key >= lim0) s[h][4 * g + e] = __float_as_uint(-INFINITY);
+                                if (key >= lim1) s[h][4 * g + 2 + e] = __float_as_uint(-INFINITY);
+                            }
                 }
-                xm[hh * kBM + row] = w_ok ? max_bits(mloc) : kXFail;
-                tc_fence_before();
-                named_barrier(pair, 64);
-                tc_fence_after();
-                const uint32_t xa = xm[row], xb = xm[kBM + row];
-                ok = __all_sync(kFullMask, xa != kXFail && xb != kXFail);  // same in both warps
-                if (!ok) {
-                    quit = true;
-                    break;
-                }
-                const float mx = fmaxf(__uint_as_float(xa), __uint_as_float(xb)) * p.qk_scale_log2;
-                // lazy rescale; warp-uniform because the O row is read and written by the
-                // whole warp (tcgen05.ld / st), and the same in both warps of the pair
-                const bool grow = mx > m_ref + kRescaleLog2;
-                if (__any_sync(kFullMask, grow)) {
-                    const float m_new = grow ? mx : m_ref;
-                    const float alpha = m_new == m_ref ? 1.f : fast_exp2(m_ref - m_new);  // 0 from -inf
-                    l *= alpha;
-                    m_ref = m_new;
-                    if (j >= 1) {  // O holds tiles < j: wait for the last P.V, then scale my columns
+                // row maxima: 32 scores per row in this lane, then over the row's four lanes
+                float a0 = -INFINITY, a1 = -INFINITY, b0 = -INFINITY, b1 = -INFINITY;
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+#pragma unroll
+                    for (int g = 0; g < 8; g += 2) {
+                        a0 = fmax3(a0, __uint_as_float(s[h][4 * g]), __uint_as_float(s[h][4 * g + 1]));
+                        b0 = fmax3(b0, __uint_as_float(s[h][4 * g + 4]), __uint_as_float(s[h][4 * g + 5]));
+                        a1 = fmax3(a1, __uint_as_float(s[h][4 * g + 2]), __uint_as_float(s[h][4 * g + 3]));
+                        b1 = fmax3(b1, __uint_as_float(s[h][4 * g + 6]), __uint_as_float(s[h][4 * g + 7]));
+                    }
+                float mx0 = fmaxf(a0, b0), mx1 = fmaxf(a1, b1);
+                mx0 = fmaxf(mx0, __shfl_xor_sync(kFullMask, mx0, 1));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(kFullMask, mx1, 1));
+                mx0 = fmaxf(mx0, __shfl_xor_sync(kFullMask, mx0, 2)) * sc;
+                mx1 = fmaxf(mx1, __shfl_xor_sync(kFullMask, mx1, 2)) * sc;
+                // lazy rescale; warp-uniform because the O rows are read and written by the
+                // whole warp (tcgen05.ld / st).  The four lanes of a row hold the same maxima.
+                const bool grow0 = mx0 > m0 + kRescaleLog2, grow1 = mx1 > m1 + kRescaleLog2;
+                if (__any_sync(kFullMask, grow0 || grow1)) {
+                    const float n0 = grow0 ? mx0 : m0, n1 = grow1 ? mx1 : m1;
+                    const float al0 = n0 == m0 ? 1.f : fast_exp2(m0 - n0);  // 0 from -inf
+                    const float al1 = n1 == m1 ? 1.f : fast_exp2(m1 - n1);
+                    l0 *= al0;
+                    l1 *= al1;
+                    m0 = n0;
+                    m1 = n1;
+                    if (j >= 1) {  // O holds tiles < j: wait for the last P.V, then scale the rows
                         ok = __all_sync(kFullMask, mbar_wait(bar(BPV + (t - 1) % kSBufs), ((t - 1) / kSBufs) & 1,
                                                              p.status));
                         if (ok) {
                             tc_fence_after();
 #pragma unroll
-                            for (int c0 = 0; c0 < DH; c0 += 32) {
-                                uint32_t r[32];
-                                tmem_ld32(tO + c0, r);
+                            for (int c0 = 0; c0 < D; c0 += 64) {
+                                uint32_t o[32];
+                                tmem_ld_16x256b<8>(tO + c0, o);
                                 tmem_wait_ld();
 #pragma unroll
-                                for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-                                tmem_st32(tO + c0, r);
+                                for (int g = 0; g < 8; ++g) {
+                                    o[4 * g] = __float_as_uint(__uint_as_float(o[4 * g]) * al0);
+                                    o[4 * g + 1] = __float_as_uint(__uint_as_float(o[4 * g + 1]) * al0);
+                                    o[4 * g + 2] = __float_as_uint(__uint_as_float(o[4 * g + 2]) * al1);
+                                    o[4 * g + 3] = __float_as_uint(__uint_as_float(o[4 * g + 3]) * al1);
+                                }
+                                tmem_st_16x256b_x8(tO + c0, o);
                             }
                             tmem_wait_st();
                         }
                     }
                 }
-                // my 64 weights, packed two per TMEM column (the P.V of this buffer's previous
-                // tile finished before this S was issued)
+                // P over the S rows (the P.V of this buffer's previous tile finished before this
+                // S was issued): the weights of keys 8j + 2(t%4), +1 pack into P column 4j + t%4
                 {
-                    const float2 sc2 = make_float2(p.qk_scale_log2, p.qk_scale_log2), nm2 = make_float2(-m_ref, -m_ref);
-                    float2 rs2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-                    uint32_t w[32];
+                    const float mb0 = m0 == -INFINITY ? 0.f : m0, mb1 = m1 == -INFINITY ? 0.f : m1;
+                    const float2 sc2 = make_float2(sc, sc);
+                    const float2 nm0 = make_float2(-mb0, -mb0), nm1 = make_float2(-mb1, -mb1);
+                    float2 rs0 = make_float2(0.f, 0.f), rs1 = make_float2(0.f, 0.f);
+                    uint32_t pw[32];
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const float2 x = __ffma2_rn(make_float2(sv[2 * i], sv[2 * i + 1]), sc2, nm2);
-                        w[i] = pack2<T>(fast_exp2(x.x), fast_exp2(x.y));
-                        rs2[i & 1] = __fadd2_rn(rs2[i & 1], unpack2<T>(w[i]));
-                    }
+                    for (int h = 0; h < 2; ++h)
+#pragma unroll
+                        for (int g = 0; g < 8; ++g) {
+                            const float2 x0 = __ffma2_rn(
+                                make_float2(__uint_as_float(s[h][4 * g]), __uint_as_float(s[h][4 * g + 1])), sc2, nm0);
+                            const float2 x1 = __ffma2_rn(
+                                make_float2(__uint_as_float(s[h][4 * g + 2]), __uint_as_float(s[h][4 * g + 3])), sc2,
+                                nm1);
+                            const uint32_t w0 = pack2<T>(fast_exp2(x0.x), fast_exp2(x0.y));
+                            const uint32_t w1 = pack2<T>(fast_exp2(x1.x), fast_exp2(x1.y));
+                            pw[2 * (h * 8 + g)] = w0;
+                            pw[2 * (h * 8 + g) + 1] = w1;
+                            rs0 = __fadd2_rn(rs0, unpack2<T>(w0));
+                            rs1 = __fadd2_rn(rs1, unpack2<T>(w1));
+                        }
                     if (ok) {
-                        tmem_st32(tS + hh * 32, w);
+                        tmem_st_16x128b_x16(tS, pw);
                         tmem_wait_st();
                     }
-                    l += (rs2[0].x + rs2[0].y) + (rs2[1].x + rs2[1].y);
+                    l0 += rs0.x + rs0.y;
+                    l1 += rs1.x + rs1.y;
                 }
                 // keys past kv_end in this tile (not loaded, or past the context): zero V rows,
                 // so that 0-weight rows never meet stale or NaN data
                 if (k0 + kBN > it.kv_end) {
                     const int valid = it.kv_end - k0, st = t % NV;
-                    ok = ok && mbar_wait(bar(BVF + st), (t / NV) & 1, p.status);
+                    ok = __all_sync(kFullMask, ok && mbar_wait(bar(BVF + st), (t / NV) & 1, p.status));
                     const uint32_t sV = sV0 + st * Sh::KV_BYTES;
                     if (ok)
                         for (int i = sidx; i < (kBN - valid) * Sh::HALVES * 8; i += 256) {
                             const int rr = valid + i / (Sh::HALVES * 8), rest = i % (Sh::HALVES * 8);
-                            sts128(sV + (rest / 8) * (kBN * 128) + rr * 128 + (rest % 8) * 16, 0u, 0u, 0u, 0u);
+                            sts128(sV + (rr / 8) * Sh::GSTR + (rest / 8) * 1024 + (rr % 8) * 128 + (rest % 8) * 16, 0u,
+                                   0u, 0u, 0u);
                         }
                     fence_async_smem();
                 }
-                named_barrier(pair, 64);  // both have read this tile's maxima
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar(BPF + sb));
+                if (ok && lane == 0) mbar_arrive(bar(BPF + sb));
+                if (!ok) break;
             }
-            if (quit) break;  // together with the partner; a later local failure goes
-                              // through the epilogue's exchange
+            if (!ok) break;
             // ---- epilogue: O / l for the rows of this chunk.  The next item's first P.V
-            // (which overwrites O) waits for P written later by these same threads.  The
-            // pair adds its two partial row sums (and exchanges the failure flag) through
-            // the exchange area (the last tile's maxima have been read by both): a barrier
-            // after the sums are written and one after they are read.
+            // (which overwrites O) waits for P written later by all eight warps, each after
+            // reading its own rows here.
             const int last = t - 1;
-            const bool e_ok = __all_sync(kFullMask, ok && mbar_wait(bar(BPV + last % kSBufs), (last / kSBufs) & 1,
-                                                                    p.status));
-            xl[hh * kBM + row] = e_ok ? l : -1.f;  // row sums are >= 0 (or NaN): -1 flags a failure
-            named_barrier(pair, 64);
-            const float la = xl[row], lb = xl[kBM + row];
-            named_barrier(pair, 64);
-            ok = __all_sync(kFullMask, la != -1.f && lb != -1.f);
+            ok = __all_sync(kFullMask, mbar_wait(bar(BPV + last % kSBufs), (last / kSBufs) & 1, p.status));
             if (!ok) break;
             tc_fence_after();
-            const float lsum = la + lb;
-            const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-            {
-                // Output rows through the 16-lane TMEM shape: lanes 4i..4i+3 hold two rows,
-                // two columns each per group of 8; one swap with the neighbouring lane gives
-                // each lane four consecutive columns, so a store instruction writes 64 (fp32)
-                // or 32 (fp16 / bf16) contiguous bytes of each of 8 rows, where one row per
-                // lane would touch 32 lines
-                const int gi = lane >> 2, ga = lane & 3;
-                const bool odd = (ga & 1) != 0;
-                auto write_rows = [&](auto out_tag) {  // one copy of the loops per output type
-                    using OT = decltype(out_tag);
-                    OT *outp = static_cast<OT *>(p.out);
+            float L0 = l0 + __shfl_xor_sync(kFullMask, l0, 1), L1 = l1 + __shfl_xor_sync(kFullMask, l1, 1);
+            L0 += __shfl_xor_sync(kFullMask, L0, 2);
+            L1 += __shfl_xor_sync(kFullMask, L1, 2);
+            const float inv0 = L0 > 0.f ? 1.f / L0 : 0.f, inv1 = L1 > 0.f ? 1.f / L1 : 0.f;
+            // Output rows straight from the 16x256b layout: one swap with the neighbouring lane
+            // gives each lane four consecutive columns, so a store instruction writes 64 (fp32)
+            // or 32 (fp16 / bf16) contiguous bytes of each of 8 rows
+            const bool odd = (ga & 1) != 0;
+            auto write_rows = [&](auto out_tag) {  // one copy of the loops per output type
+                using OT = decltype(out_tag);
+                OT *outp = static_cast<OT *>(p.out);
 #pragma unroll
-                    for (int slab = 0; slab < 2; ++slab) {
-                        uint32_t r[DH / 2];
-                        tmem_ld_16x256b<DH / 8>(tmem + ((uint32_t)(quarter * 32 + slab * 16) << 16) + kTmemO + hh * DH, r);
-                        tmem_wait_ld();
+                for (int c0 = 0; c0 < D; c0 += 64) {
+                    uint32_t r[32];
+                    tmem_ld_16x256b<8>(tO + c0, r);
+                    tmem_wait_ld();
 #pragma unroll
-                        for (int rh = 0; rh < 2; ++rh) {  // rows slab*16 + gi and slab*16 + 8 + gi of the quarter
-                            const int qrow = slab * 16 + rh * 8 + gi, trow = quarter * 32 + qrow;
-                            const float rinv = __shfl_sync(kFullMask, inv, qrow);
-                            const int rtok = it.tok_begin + trow / G;
-                            const int64_t obase = ((int64_t)(it.q0 + rtok) * Hq + it.g * G + trow % G) * D + hh * DH;
+                    for (int rh = 0; rh < 2; ++rh) {
+                        const int trow = rh ? row1 : row0;
+                        const float rinv = rh ? inv1 : inv0;
+                        const int rtok = it.tok_begin + trow / G;
+                        const int64_t obase = ((int64_t)(it.q0 + rtok) * Hq + it.g * G + trow % G) * D + c0;
 #pragma unroll
-                            for (int j = 0; j < DH / 8; j += 2) {
-                                const int e0 = 4 * j + 2 * rh, e1 = 4 * (j + 1) + 2 * rh;  // this row's pair in groups j, j+1
-                                const float2 keep = odd ? make_float2(__uint_as_float(r[e1]), __uint_as_float(r[e1 + 1]))
-                                                        : make_float2(__uint_as_float(r[e0]), __uint_as_float(r[e0 + 1]));
-                                const float2 send = odd ? make_float2(__uint_as_float(r[e0]), __uint_as_float(r[e0 + 1]))
-                                                        : make_float2(__uint_as_float(r[e1]), __uint_as_float(r[e1 + 1]));
-                                const float2 got = make_float2(__shfl_xor_sync(kFullMask, send.x, 1),
-                                                               __shfl_xor_sync(kFullMask, send.y, 1));
-                                const int col = odd ? 8 * (j + 1) + 2 * (ga - 1) : 8 * j + 2 * ga;
-                                const float4 v = odd ? make_float4(got.x * rinv, got.y * rinv, keep.x * rinv, keep.y * rinv)
-                                                     : make_float4(keep.x * rinv, keep.y * rinv, got.x * rinv, got.y * rinv);
-                                if (rtok >= it.Lq) continue;
-                                if constexpr (std::is_same<OT, float>::value) {
-                                    *reinterpret_cast<float4 *>(outp + obase + col) = v;
-                                } else if constexpr (std::is_same<OT, __half>::value) {
-                                    __half2 lo = __floats2half2_rn(v.x, v.y), hi = __floats2half2_rn(v.z, v.w);
-                                    *reinterpret_cast<uint2 *>(outp + obase + col) =
-                                        make_uint2(*reinterpret_cast<uint32_t *>(&lo), *reinterpret_cast<uint32_t *>(&hi));
-                                } else {
-                                    __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
-                                    *reinterpret_cast<uint2 *>(outp + obase + col) =
-                                        make_uint2(*reinterpret_cast<uint32_t *>(&lo), *reinterpret_cast<uint32_t *>(&hi));
-                                }
+                        for (int g = 0; g < 8; g += 2) {
+                            const int e0 = 4 * g + 2 * rh, e1 = 4 * (g + 1) + 2 * rh;  // this row's pair in groups g, g+1
+                            const float2 keep = odd ? make_float2(__uint_as_float(r[e1]), __uint_as_float(r[e1 + 1]))
+                                                    : make_float2(__uint_as_float(r[e0]), __uint_as_float(r[e0 + 1]));
+                            const float2 send = odd ? make_float2(__uint_as_float(r[e0]), __uint_as_float(r[e0 + 1]))
+                                                    : make_float2(__uint_as_float(r[e1]), __uint_as_float(r[e1 + 1]));
+                            const float2 got = make_float2(__shfl_xor_sync(kFullMask, send.x, 1),
+                                                           __shfl_xor_sync(kFullMask, send.y, 1));
+                            const int col = odd ? 8 * (g + 1) + 2 * (ga - 1) : 8 * g + 2 * ga;
+                            const float4 v = odd ? make_float4(got.x * rinv, got.y * rinv, keep.x * rinv, keep.y * rinv)
+                                                 : make_float4(keep.x * rinv, keep.y * rinv, got.x * rinv, got.y * rinv);
+                            if (rtok >= it.Lq) continue;
+                            if constexpr (std::is_same<OT, float>::value) {
+                                *reinterpret_cast<float4 *>(outp + obase + col) = v;
+                            } else if constexpr (std::is_same<OT, __half>::value) {
+                                __half2 lo = __floats2half2_rn(v.x, v.y), hi = __floats2half2_rn(v.z, v.w);
+                                *reinterpret_cast<uint2 *>(outp + obase + col) =
+                                    make_uint2(*reinterpret_cast<uint32_t *>(&lo), *reinterpret_cast<uint32_t *>(&hi));
+                            } else {
+                                __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
+                                *reinterpret_cast<uint2 *>(outp + obase + col) =
+                                    make_uint2(*reinterpret_cast<uint32_t *>(&lo), *reinterpret_cast<uint32_t *>(&hi));
                             }
                         }
                     }
-                };
-                if (p.out_dtype == PA_F32)
-                    write_rows(float{});
-                else if (p.out_dtype == PA_F16)
-                    write_rows(__half{});
-                else
-                    write_rows(__nv_bfloat16{});
-            }
+                }
+            };
+            if (p.out_dtype == PA_F32)
+                write_rows(float{});
+            else if (p.out_dtype == PA_F16)
+                write_rows(__half{});
+            else
+                write_rows(__nv_bfloat16{});
             tc_fence_before();
         }
         if (!ok) *abort_v = 1;
@@ -917,16 +902,16 @@ int launch_prefill(const PrefillArgs &a) {
     const int G = a.num_heads / a.num_kv_heads;
     const int64_t pool_rows = (int64_t)a.num_blocks * a.block_size;
     if (pool_rows <= 0 || pool_rows > INT32_MAX) return PA_ERR_INVALID_ARG;
-    // Boxes are 64 elements (128 bytes, the swizzle span) wide along D.  Q boxes
-    // cover the G heads of one kv head for 128/G tokens; K/V boxes one block of
-    // one kv head.
+    // Q boxes are 64 elements (128 bytes, the swizzle span) wide along D and cover the G
+    // heads of one kv head for 128/G tokens; a K/V box is one whole block of one kv head,
+    // all of D in 64-wide slices (one copy per block).
     CUtensorMap qm, km, vm;
     if (make_tensor_map_3d(&qm, a.query, a.kv_dtype, a.head_dim, a.num_heads, a.num_tokens, 64, G,
                            kBM / G, true) != PA_OK ||
-        make_tensor_map_3d(&km, a.key_cache, a.kv_dtype, a.head_dim, a.num_kv_heads, pool_rows, 64, 1,
-                           a.block_size, true) != PA_OK ||
-        make_tensor_map_3d(&vm, a.value_cache, a.kv_dtype, a.head_dim, a.num_kv_heads, pool_rows, 64, 1,
-                           a.block_size, true) != PA_OK)
+        make_kv_block_map(&km, a.key_cache, a.kv_dtype, a.head_dim, a.num_kv_heads, pool_rows, a.block_size) !=
+            PA_OK ||
+        make_kv_block_map(&vm, a.value_cache, a.kv_dtype, a.head_dim, a.num_kv_heads, pool_rows, a.block_size) !=
+            PA_OK)
         return PA_ERR_CUDA;
     switch (a.kv_dtype) {
         case PA_F16: return dispatch_d<F16>(prm, a.head_dim, G, qm, km, vm, a.max_query_len, a.num_seqs, a.stream);

@@ -103,6 +103,16 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// 5-D tiled TMA load into shared memory, completing on `bar` (transaction bytes).
+__device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap *map, int c0, int c1, int c2,
+                                            int c3, int c4, uint32_t bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(bar), "l"(policy)
+        : "memory");
+}
+
 // 3-D tiled TMA load into shared memory, completing on `bar` (transaction bytes).
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int c0, int c1,
                                             int c2, uint32_t bar, uint64_t policy) {
@@ -123,6 +133,16 @@ __device__ __forceinline__ void named_barrier(int id, int threads) {
 // {D, box_heads, box_rows}.  Returns PA_OK or PA_ERR_CUDA.
 int make_kv_tensor_map(CUtensorMap *map, const void *base, pa_dtype dtype, int head_dim,
                        int num_kv_heads, int64_t rows, int box_heads, int box_rows);
+
+// 5-D tensor map over a KV pool [rows][Hkv][D] (16-bit elements, D a multiple of 64, rows
+// and the block size multiples of 8) whose box is one block of one kv head: dimensions
+// (column in a 64-wide slice of D, row in a group of 8, slice, group of 8 rows, kv head),
+// box {64, 8, D/64, block_size/8, 1}, 128-byte swizzle.  In shared memory the box is
+// [group][slice][8 rows][128 B]: every 8-row slab of a slice is one swizzle atom, so the
+// block's rows form K-major (and MN-major) operands whose 8-row groups are 1024 * D/64
+// bytes apart.  One copy per block instead of one per slice.
+int make_kv_block_map(CUtensorMap *map, const void *base, pa_dtype dtype, int head_dim, int num_kv_heads,
+                      int64_t rows, int block_size);
 
 // General 3-D tensor map [dim2][dim1][dim0] (dim0 innermost, dense) with box
 // {box0, box1, box2}; 128-byte swizzle when asked (box0 * element size must then

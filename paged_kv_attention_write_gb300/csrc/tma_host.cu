@@ -41,6 +41,22 @@ int make_tensor_map_3d(CUtensorMap *map, const void *base, pa_dtype dtype, int d
     return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
 }
 
+int make_kv_block_map(CUtensorMap *map, const void *base, pa_dtype dtype, int head_dim, int num_kv_heads,
+                      int64_t rows, int block_size) {
+    auto fn = encode_fn();
+    if (!fn || head_dim % 64 != 0 || rows % 8 != 0 || block_size % 8 != 0) return PA_ERR_CUDA;
+    CUtensorMapDataType dt = dtype == PA_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const cuuint64_t row_bytes = (cuuint64_t)num_kv_heads * head_dim * 2;
+    // (column in a 64-wide slice, row in a group of 8, slice, group, kv head)
+    cuuint64_t dims[5] = {64, 8, (cuuint64_t)head_dim / 64, (cuuint64_t)rows / 8, (cuuint64_t)num_kv_heads};
+    cuuint64_t strides[4] = {row_bytes, 128, 8 * row_bytes, (cuuint64_t)head_dim * 2};
+    cuuint32_t box[5] = {64, 8, (cuuint32_t)head_dim / 64, (cuuint32_t)block_size / 8, 1};
+    cuuint32_t estride[5] = {1, 1, 1, 1, 1};
+    CUresult r = fn(map, dt, 5, const_cast<void *>(base), dims, strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
+}
+
 int make_kv_tensor_map(CUtensorMap *map, const void *base, pa_dtype dtype, int head_dim,
                        int num_kv_heads, int64_t rows, int box_heads, int box_rows) {
     return make_tensor_map_3d(map, base, dtype, head_dim, num_kv_heads, rows, head_dim, box_heads,
