@@ -392,13 +392,6 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
         prefetch_tensormap(&kmap);
         prefetch_tensormap(&vmap);
     }
-    if (warp == NW) {  // the block tables (spread over the CTAs) and the context lengths into L2
-        const int64_t bt_lines = ((int64_t)p.num_seqs * p.max_blocks_per_seq * 4 + 127) / 128;
-        const int lines = bt_lines < (1 << 30) ? (int)bt_lines : (1 << 30);
-        for (int i = blockIdx.x * 32 + lane; i < lines; i += gridDim.x * 32)
-            prefetch_l2(reinterpret_cast<const char *>(p.block_tables) + (int64_t)i * 128);
-        if (lane * 32 < p.num_seqs) prefetch_l2(p.context_lens + lane * 32);
-    }
     pdl_wait_previous();      // context lengths, block tables, caches (and the plan) are ready
     pdl_launch_dependents();  // the reduce kernel may launch; it waits for our completion
 

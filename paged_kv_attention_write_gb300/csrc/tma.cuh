@@ -92,13 +92,6 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
     return pol;
 }
 
-// Pull one line into L2 (a hint: it reads nothing into registers, so data that an
-// earlier kernel writes afterwards is still what later loads see, L2 being the point of
-// coherence).
-__device__ __forceinline__ void prefetch_l2(const void *p) {
-    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
-}
-
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
