@@ -712,7 +712,9 @@ def mixed_batch_measurement(device, flush, hbm_peak, tc_peak):
 
 
 def secondary_measurements(device, flush, hbm_peak, tc_peak, peak_kind):
-    """Shorter timings of the other hot-path rows: decode batch, chunked prefill, block copy."""
+    """Shorter timings of the other hot-path rows: decode batch, chunked prefill, cache write,
+    RoPE variants, mixed batch, host manager and scheduler replay, block copy, and decode on
+    the stress workload (block 16, bf16)."""
     import paged_kv_attention_write_gb300 as pa
     res = {}
     case = workloads.decode_batch()
@@ -774,6 +776,18 @@ def secondary_measurements(device, flush, hbm_peak, tc_peak, peak_kind):
     cb = int(bm.shape[0]) * case.block_size * case.num_kv_heads * case.head_dim * 2 * 2 * 2
     res["copy_blocks_stress"] = {"pairs": int(bm.shape[0]), "ms": round(t, 5),
                                  "GB/s": round(cb / (t * 1e-3) / 1e9, 1)}
+    # decode on the same stress workload (256 sequences, log-uniform lengths, 20 % free blocks)
+    del kc, vc, bm
+    st = DecodeStep(case, device)
+    st.reshape()
+    for _ in range(3):
+        st.decode()
+    ms, _ = time_steps(st.decode, 30, flush, False)
+    t = statistics.mean(ms)
+    b = decode_bytes(case)["decode"]
+    res["stress_decode"] = {"workload": case.name, "ms": round(t, 5), "GB/s": round(b / t / 1e6, 1),
+                            "frac_hbm": round(b / t / 1e6 / hbm_peak, 4),
+                            "seq_steps_per_s": round(case.num_seqs / t * 1e3, 1)}
     return res
 
 
