@@ -219,6 +219,41 @@ def test_prefill_single_row_matches_decode(oracle_mod):
     assert (out.cpu() - od).abs().max().item() < 5e-3
 
 
+# ----------------------------------------------------------------------------- moving reference max
+
+def _keys_growing_with_position(case, rate=1.0 / 8):
+    """Scale every key (cached and fresh) by 1 + rate * position.  A row's scores then grow
+    along its context by far more than the 2^8 that the lazily rescaled running max lets
+    pass, so the reference moves inside rows, tile after tile, and the kernels rescale the
+    output accumulated so far; with N(0,1) keys that path never runs."""
+    kc, bt, bs = case.key_cache, case.block_tables, case.block_size
+    for s in range(case.num_seqs):
+        for j in range(int(case.cached_lens[s])):
+            b, o = int(bt[s, j // bs]), j % bs
+            kc[b, o] = (kc[b, o].double() * (1 + rate * j)).to(kc.dtype)
+    if case.is_decode:
+        pos = [int(n) for n in case.cached_lens]
+    else:
+        qsl = case.query_start_loc.tolist()
+        pos = [int(case.cached_lens[s]) + i for s in range(case.num_seqs) for i in range(qsl[s + 1] - qsl[s])]
+    for t, ps in enumerate(pos):
+        case.new_key[t] = (case.new_key[t].double() * (1 + rate * ps)).to(case.new_key.dtype)
+    return case
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16], ids=["bf16", "fp16"])
+def test_prefill_running_max_moves_across_tiles(oracle_mod, dtype):
+    case = workloads.make_prefill_case("pf-grow", [0, 300, 1000], [200, 130, 64], 16, 8, 2, 128, dtype,
+                                       seed=31)
+    check_case(_keys_growing_with_position(case), oracle_mod)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16, torch.float32], ids=["bf16", "fp16", "fp32"])
+def test_decode_running_max_moves_across_tiles(oracle_mod, dtype):
+    case = workloads.make_decode_case("dec-grow", [100, 700, 2000], 16, 8, 2, 128, dtype, seed=32)
+    check_case(_keys_growing_with_position(case), oracle_mod)
+
+
 # ----------------------------------------------------------------------------- device-side range checks
 
 def test_device_checks_report_instead_of_reading_out_of_range():
