@@ -80,14 +80,23 @@ def prefill_work(case) -> tuple[float, int]:
     return flops, byts
 
 
+def _code_only(text: str) -> str:
+    """Source text without comments and blank lines (comments do not change a kernel)."""
+    import re
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    lines = (re.sub(r"//.*$", "", ln).rstrip() for ln in text.splitlines())
+    return "\n".join(ln for ln in lines if ln)
+
+
 def kernel_source_hash(kind: str = "decode") -> str:
-    """Hash of the CUDA sources a kernel is built from (ties ncu counters to a kernel version)."""
+    """Hash of the code of the CUDA sources a kernel is built from, comments left out (ties
+    ncu counters to a kernel version)."""
     csrc = ROOT / "paged_kv_attention_write_gb300" / "csrc"
     files = {"decode": ["decode_kernels.cuh", "decode.cu", "tma.cuh", "common.cuh"],
              "prefill": ["prefill.cu", "tma.cuh", "common.cuh"]}[kind]
     h = hashlib.sha256()
     for f in files:
-        h.update((csrc / f).read_bytes())
+        h.update(_code_only((csrc / f).read_text()).encode())
     return h.hexdigest()[:16]
 
 

@@ -24,11 +24,11 @@
 // Per 128-key tile j:
 //   S_j = Q K_j^T   tcgen05.mma M128 N128 K=D, fp32 in TMEM (three buffers, so
 //                   the S products run up to three tiles ahead)
-//   P_j             one thread per row reads its S row from TMEM: mask,
-//                   online softmax in the log2 domain with lazy rescaling
-//                   (the reference max moves only when a score exceeds it by
-//                   2^8), P_j rounded to bf16/fp16 and written back to TMEM
-//                   over the S row
+//   P_j             the softmax warps read S from TMEM (a row spread over
+//                   four lanes): mask, online softmax in the log2 domain with
+//                   lazy rescaling (the reference max moves only when a score
+//                   exceeds it by 2^8), P_j rounded to bf16/fp16 and written
+//                   back to TMEM over the S row
 //   O  += P_j V_j   tcgen05.mma M128 N=D K128 with A = P from TMEM, fp32 in
 //                   TMEM; V is the MN-major shared-memory operand
 // Warp roles: warps 0 and 2 issue the TMA loads (the Q tile; per key tile one
