@@ -260,8 +260,11 @@ class DecodeStep:
         return self.h_out.numel() * self.h_out.element_size()
 
     def launches_per_step(self):
-        # pa_reshape_and_cache: 1 kernel; pa_decode: plan, split, reduce
-        return 4
+        # pa_reshape_and_cache: 1 kernel; pa_decode: split + reduce, and a plan kernel
+        # first when there are 2048 or more (kv-head group, sequence) segments
+        c = self.case
+        segments = max(1, c.num_kv_heads // 8) * c.num_seqs
+        return 3 + (1 if segments >= 2048 else 0)
 
 
 class PrefillStep:
@@ -329,9 +332,9 @@ def prefill_arm(args, case, device, rank, world, dist_on):
     with ClockSampler(device.index) as clocks:
         step_ms, wall = time_steps(st.step, args.steps, flush, dist_on)
     e2e_ms, _ = time_steps(st.e2e_step, max(3, args.steps // 4), flush, dist_on)
-    ms_step = _max_over_ranks(statistics.mean(step_ms), dist_on)
-    ms_pf = _max_over_ranks(statistics.mean(pf_ms), dist_on)
-    ms_e2e = _max_over_ranks(statistics.mean(e2e_ms), dist_on)
+    ms_step = _max_over_ranks(statistics.median(step_ms), dist_on)
+    ms_pf = _max_over_ranks(statistics.median(pf_ms), dist_on)
+    ms_e2e = _max_over_ranks(statistics.median(e2e_ms), dist_on)
     if rank != 0:
         return None
     tfs = flops / (ms_pf * 1e-3) / 1e12
@@ -359,6 +362,8 @@ def prefill_arm(args, case, device, rank, world, dist_on):
                 "ms_per_step": round(ms_e2e, 5), "h2d_bytes_per_step": st.h_in.numel(),
                 "d2h_bytes_per_step": st.h_out.numel() * 4},
         "gpu_launches": args.steps * 2,
+        "step_ms": {"step": step_stats(step_ms), "pa_prefill_chunk": step_stats(pf_ms), "e2e": step_stats(e2e_ms),
+                    "statistic": "median of the per-step CUDA-event times (p10 / p90 / mean beside it)"},
         "clocks": clocks.summary(),
         "timed_region_s": round(wall, 3),
     }
@@ -408,6 +413,13 @@ def time_steps(fn, steps, flush, dist_on):
     return ms, wall
 
 
+def step_stats(ms) -> dict:
+    """Median and spread of per-step device times (ms): the median is the figure used."""
+    q = np.percentile(np.asarray(ms, dtype=np.float64), [10, 50, 90])
+    return {"median": round(float(q[1]), 5), "p10": round(float(q[0]), 5), "p90": round(float(q[2]), 5),
+            "mean": round(float(np.mean(ms)), 5), "n": len(ms)}
+
+
 def gpu_arm(args, rank, world, dist_on):
     device = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(device)
@@ -432,9 +444,9 @@ def gpu_arm(args, rank, world, dist_on):
     torch.cuda.synchronize()
     e2e_ms, _ = time_steps(st.e2e_step, max(3, args.steps // 4), flush, dist_on)
 
-    ms_step = _max_over_ranks(statistics.mean(step_ms), dist_on)
-    ms_dec = _max_over_ranks(statistics.mean(dec_ms), dist_on)
-    ms_e2e = _max_over_ranks(statistics.mean(e2e_ms), dist_on)
+    ms_step = _max_over_ranks(statistics.median(step_ms), dist_on)
+    ms_dec = _max_over_ranks(statistics.median(dec_ms), dist_on)
+    ms_e2e = _max_over_ranks(statistics.median(e2e_ms), dist_on)
     value = world * byts["step"] / (ms_step * 1e-3) / 1e9
     dec_gbs = byts["decode"] / (ms_dec * 1e-3) / 1e9
     e2e_gbs = world * byts["step"] / (ms_e2e * 1e-3) / 1e9
@@ -492,6 +504,8 @@ def gpu_arm(args, rank, world, dist_on):
         "e2e": {"value": round(e2e_gbs, 2), "unit": "GB/s", "ms_per_step": round(ms_e2e, 5),
                 "h2d_bytes_per_step": st.h2d_bytes(), "d2h_bytes_per_step": st.d2h_bytes()},
         "gpu_launches": args.steps * st.launches_per_step(),
+        "step_ms": {"step": step_stats(step_ms), "pa_decode": step_stats(dec_ms), "e2e": step_stats(e2e_ms),
+                    "statistic": "median of the per-step CUDA-event times (p10 / p90 / mean beside it)"},
         "clocks": clocks.summary(),
         "timed_region_s": round(wall, 3),
     }
@@ -658,7 +672,7 @@ def rope_measurement(device, flush, hbm_peak):
                      ("reshape_and_cache_rope", lambda: pa.pa_reshape_and_cache_rope(nk, nv, kc, vc, sl, pos, rope))):
         for _ in range(3):
             fn()
-        t = statistics.mean(time_steps(fn, 50, flush, False)[0])
+        t = statistics.median(time_steps(fn, 50, flush, False)[0])
         res[name + "_2048_tokens"] = {"ms": round(t, 5), "GB/s": round(rb / (t * 1e-3) / 1e9, 1)}
     del kc, vc
     case = workloads.decode_batch()
@@ -670,7 +684,7 @@ def rope_measurement(device, flush, hbm_peak):
                                                                case.scale, rope, workspace=st.ws))):
         for _ in range(3):
             fn()
-        t = statistics.mean(time_steps(fn, 50, flush, False)[0])
+        t = statistics.median(time_steps(fn, 50, flush, False)[0])
         res[name + "_decode_batch"] = {"ms": round(t, 5), "GB/s": round(b / t / 1e6, 1),
                                        "frac_hbm": round(b / t / 1e6 / hbm_peak, 4)}
     res["workloads"] = "cache write: prefill_chunk's 2048 tokens; decode: decode_batch (32 sequences)"
@@ -709,8 +723,8 @@ def mixed_batch_measurement(device, flush, hbm_peak, tc_peak):
     for _ in range(5):
         mixed()
         split()
-    t_mix = statistics.mean(time_steps(mixed, 50, flush, False)[0])
-    t_split = statistics.mean(time_steps(split, 50, flush, False)[0])
+    t_mix = statistics.median(time_steps(mixed, 50, flush, False)[0])
+    t_split = statistics.median(time_steps(split, 50, flush, False)[0])
     flops, byts = prefill_work(case)
     t_roof = max(flops / (tc_peak * 1e12), byts / (hbm_peak * 1e9)) * 1e3
     return {"workload": case.name, "decode_rows": nd, "chunks": case.num_seqs - nd,
@@ -732,7 +746,7 @@ def secondary_measurements(device, flush, hbm_peak, tc_peak, peak_kind):
         st.step()
     ms, _ = time_steps(st.decode, 50, flush, False)
     b = decode_bytes(case)["decode"]
-    t = statistics.mean(ms)
+    t = statistics.median(ms)
     res["decode_batch"] = {"workload": case.name, "ms": round(t, 5),
                            "GB/s": round(b / t / 1e6, 1), "frac_hbm": round(b / t / 1e6 / hbm_peak, 4),
                            "seq_steps_per_s": round(case.num_seqs / t * 1e3, 1)}
@@ -751,7 +765,7 @@ def secondary_measurements(device, flush, hbm_peak, tc_peak, peak_kind):
     for _ in range(5):
         prefill()
     ms, _ = time_steps(prefill, 50, flush, False)
-    t = statistics.mean(ms)
+    t = statistics.median(ms)
     flops, byts = prefill_work(case)
     tfs = flops / (t * 1e-3) / 1e12
     res["prefill_chunk"] = {"workload": case.name, "ms": round(t, 5), "TFLOP/s": round(tfs, 1),
@@ -763,7 +777,7 @@ def secondary_measurements(device, flush, hbm_peak, tc_peak, peak_kind):
     def reshape():
         pa.pa_reshape_and_cache(nk, nv, kc, vc, sl)
     ms, _ = time_steps(reshape, 50, flush, False)
-    t = statistics.mean(ms)
+    t = statistics.median(ms)
     rb = nk.numel() * nk.element_size() * 4 + sl.numel() * 8
     res["reshape_and_cache_2048_tokens"] = {"ms": round(t, 5), "GB/s": round(rb / (t * 1e-3) / 1e9, 1)}
     del kc, vc
@@ -772,7 +786,7 @@ def secondary_measurements(device, flush, hbm_peak, tc_peak, peak_kind):
     res["kv_manager"] = manager_measurement()
     res["serve_replay"] = serve_replay_measurement(device)
     # block copy: 26 recipients' leading blocks of the stress workload (bs 16, bf16)
-    case = workloads.stress_decode(block_size=16, dtype=torch.bfloat16)
+    stress16 = case = workloads.stress_decode(block_size=16, dtype=torch.bfloat16)
     kc, vc = case.key_cache.to(device), case.value_cache.to(device)
     bm = case.block_mapping.to(device)
 
@@ -781,22 +795,33 @@ def secondary_measurements(device, flush, hbm_peak, tc_peak, peak_kind):
     for _ in range(3):
         copy()
     ms, _ = time_steps(copy, 50, flush, False)
-    t = statistics.mean(ms)
+    t = statistics.median(ms)
     cb = int(bm.shape[0]) * case.block_size * case.num_kv_heads * case.head_dim * 2 * 2 * 2
     res["copy_blocks_stress"] = {"pairs": int(bm.shape[0]), "ms": round(t, 5),
                                  "GB/s": round(cb / (t * 1e-3) / 1e9, 1)}
-    # decode on the same stress workload (256 sequences, log-uniform lengths, 20 % free blocks)
     del kc, vc, bm
-    st = DecodeStep(case, device)
-    st.reshape()
-    for _ in range(3):
-        st.decode()
-    ms, _ = time_steps(st.decode, 30, flush, False)
-    t = statistics.mean(ms)
-    b = decode_bytes(case)["decode"]
-    res["stress_decode"] = {"workload": case.name, "ms": round(t, 5), "GB/s": round(b / t / 1e6, 1),
-                            "frac_hbm": round(b / t / 1e6 / hbm_peak, 4),
-                            "seq_steps_per_s": round(case.num_seqs / t * 1e3, 1)}
+    # decode on the stress workload (256 sequences, log-uniform lengths, 20 % free blocks,
+    # prefix copies) for every block size and cache dtype
+    res["stress_decode"] = {}
+    for bs in (8, 16, 32):
+        for dt, tag in ((torch.float16, "fp16"), (torch.bfloat16, "bf16")):
+            case = stress16 if (bs == 16 and dt == torch.bfloat16) else \
+                workloads.stress_decode(block_size=bs, dtype=dt)
+            st = DecodeStep(case, device)
+            if case.block_mapping is not None:
+                pa.pa_copy_blocks(st.kc, st.vc, case.block_mapping.to(device))
+            st.reshape()
+            for _ in range(3):
+                st.decode()
+            ms, _ = time_steps(st.decode, 30, flush, False)
+            t = statistics.median(ms)
+            b = decode_bytes(case)["decode"]
+            res["stress_decode"][f"bs{bs}_{tag}"] = {
+                "workload": case.name, "ms": round(t, 5), "GB/s": round(b / t / 1e6, 1),
+                "frac_hbm": round(b / t / 1e6 / hbm_peak, 4),
+                "seq_steps_per_s": round(case.num_seqs / t * 1e3, 1)}
+            del st
+            torch.cuda.empty_cache()
     return res
 
 
@@ -822,7 +847,78 @@ def cpu_baseline(case, byts, reps: int = 2):
     return {"value": round(byts["step"] / t / 1e9, 4), "unit": "GB/s", "cores": oracle.num_threads(),
             "kind": "oracle", "seconds_per_step": round(t, 3),
             "sample": f"{reps} whole steps of the same workload ({case.num_seqs} sequences, all heads), median",
+            "per_workload": {"decode_batch": oracle_decode_timing("decode_batch", reps),
+                             "decode_batch_single_thread": oracle_single_thread("decode_batch", reps),
+                             "prefill_chunk": oracle_prefill_timing()},
             "kv_manager_reference": reference_manager_measurement()}
+
+
+def oracle_decode_timing(workload: str, reps: int = 2) -> dict:
+    """The oracle on whole decode steps of a workload (cache write + attention), median."""
+    import oracle
+    oracle.build()
+    case = workloads.WORKLOADS[workload]()
+    kc, vc = case.key_cache.clone(), case.value_cache.clone()
+    times = []
+    for _ in range(reps):
+        t0 = time.perf_counter()
+        _oracle_step(oracle, case, kc, vc)
+        times.append(time.perf_counter() - t0)
+    t = statistics.median(times)
+    b = decode_bytes(case)["step"]
+    return {"value": round(b / t / 1e9, 4), "unit": "GB/s", "cores": oracle.num_threads(),
+            "seconds_per_step": round(t, 3), "seq_steps_per_s": round(case.num_seqs / t, 2),
+            "sample": f"{reps} whole steps of {case.name}, median"}
+
+
+def oracle_single_thread(workload: str, reps: int = 2) -> dict:
+    """oracle_decode_timing with one thread: a child process started with OMP_NUM_THREADS=1
+    (the oracle's thread count is fixed when its library loads)."""
+    code = (f"import sys, json; sys.path.insert(0, {str(ROOT)!r}); import bench; "
+            f"print(json.dumps(bench.oracle_decode_timing({workload!r}, {reps})))")
+    env = {**os.environ, "OMP_NUM_THREADS": "1"}
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env,
+                       timeout=900, cwd=str(ROOT))
+    if r.returncode != 0:
+        return {"error": (r.stderr or r.stdout).strip().splitlines()[-1:]}
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def oracle_prefill_timing(budget_s: float = 8.0) -> dict:
+    """The oracle on a bounded sample of the chunked-prefill workload: the last R rows of
+    every sequence's chunk (all heads), R chosen so that one run takes about budget_s."""
+    import oracle
+    oracle.build()
+    case = workloads.prefill_chunk()
+    kc, vc = case.key_cache.clone(), case.value_cache.clone()
+    oracle.reshape_and_cache(case.new_key, case.new_value, kc, vc, case.slot_mapping, case.block_size)
+    qsl = case.query_start_loc.tolist()
+
+    def sub_case(rows):
+        sub = workloads.PagedCase(**{**case.__dict__})
+        idx = torch.cat([torch.arange(qsl[s + 1] - min(rows, qsl[s + 1] - qsl[s]), qsl[s + 1])
+                         for s in range(case.num_seqs)])
+        sub.query = case.query[idx].contiguous()
+        lens = [min(rows, qsl[s + 1] - qsl[s]) for s in range(case.num_seqs)]
+        sub.query_start_loc = torch.tensor([0] + list(np.cumsum(lens)), dtype=torch.int32)
+        return sub
+
+    def run(sub):
+        t0 = time.perf_counter()
+        oracle.paged_attention(sub.query, sub.query_start_loc, kc, vc, sub.block_tables,
+                               sub.context_lens, case.scale)
+        return time.perf_counter() - t0
+
+    probe = sub_case(2)
+    per_row = run(probe) / 2
+    lq = max(qsl[s + 1] - qsl[s] for s in range(case.num_seqs))
+    rows = int(max(1, min(lq, budget_s / max(per_row, 1e-9))))
+    sub = sub_case(rows)
+    t = run(sub)
+    flops, _ = prefill_work(sub)
+    return {"value": round(flops / t / 1e12, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(),
+            "seconds": round(t, 3),
+            "sample": f"last {rows} chunk rows of each of the {case.num_seqs} sequences of {case.name}, all heads"}
 
 
 def reference_manager_measurement():
@@ -878,7 +974,7 @@ def reference_arm(args, rank, world, budget_s: float = 150.0):
         t0 = time.perf_counter()
         _oracle_step(oracle, sub, kc, vc)
         times.append(time.perf_counter() - t0)
-    t = statistics.mean(times)
+    t = statistics.median(times)
     value = sb["step"] / t / 1e9
     desc = (f"first sequence of {case.num_seqs}, all {case.num_heads} heads, context truncated "
             f"to its first {tokens} of {full} tokens, per step")
@@ -928,7 +1024,7 @@ def reference_prefill(args, case, world, budget_s: float = 150.0):
         t0 = time.perf_counter()
         run(sub)
         times.append(time.perf_counter() - t0)
-    t = statistics.mean(times)
+    t = statistics.median(times)
     value = flops / t / 1e12
     desc = f"last {rows} of the first sequence's {lq} chunk rows, all heads, per step"
     return {

@@ -24,6 +24,11 @@
  *  - The return value is PA_OK (0) or a negative PA_ERR_* code.  Argument
  *    errors are detected on the host before anything is launched.  A failed
  *    launch returns PA_ERR_CUDA.
+ *  - The first call of pa_decode, pa_decode_rope, pa_decode_noalloc or
+ *    pa_prefill_chunk on a device raises its kernels' shared-memory limit
+ *    (cudaFuncSetAttribute) and may load the library's device code into the
+ *    current context; make that first call outside stream capture.  Calls
+ *    from several host threads are safe (per-device setup is atomic).
  *  - Values that only the device can see (slot numbers, block ids, context
  *    lengths) are range-checked inside the kernels: an out-of-range value is
  *    never dereferenced; the offending token / block is skipped and, if
@@ -156,9 +161,11 @@ int pa_decode(void *out, pa_dtype out_dtype, const void *query, const void *key_
  * anything runs; with 152 SMs, Hq = 32, Hkv = 8 and D = 128 that allows about 350
  * sequences.  Nothing is allocated and nothing needs clearing between calls.
  *
- * The first call on each device looks up the array's device address
- * (cudaGetSymbolAddress); make that first call before any stream capture.
- * All calls on a device share the one array: two calls whose kernels overlap
+ * Every call looks up the array's device address in the current context
+ * (cudaGetSymbolAddress), so the address never goes stale across device resets
+ * or contexts.  The first call in a context loads the library's device code
+ * there and sets up the decode kernels: make that first call before any stream
+ * capture.  All calls on a device share the one array: two calls whose kernels overlap
  * on the GPU (different streams, no ordering between them) race and corrupt
  * each other's results.
  */

@@ -10,37 +10,56 @@
 // Both are HBM-bound bit copies: 16-byte vector loads and stores, coalesced
 // along the row; no arithmetic on the elements.  A third kernel writes the cache with
 // the key rotated (RoPE) on the way in.
-#include "common.cuh"
+#include "tma.cuh"  // device_sm_count
 
 namespace pa {
 namespace {
 
 constexpr int kCopyThreads = 128;
+constexpr int kWriteThreads = 256;
+constexpr int kWriteUnroll = 4;  // 16-byte K and V vectors per thread in flight at once
 
-// One CTA per fresh token; the row is row_bytes (a multiple of 16).
-__global__ void __launch_bounds__(kCopyThreads)
+// The fresh rows seen as one flat list of 16-byte vectors (token t owns vectors
+// t*vecs_per_row .. +vecs_per_row-1).  Each thread takes kWriteUnroll vectors a grid stride
+// apart and issues every load -- K, V and the slot of its token -- before any store, so a
+// CTA keeps 32 KB in flight and the kernel costs one round trip for the loads and one for
+// the stores (the loads do not depend on the slot; only the stores do).
+__global__ void __launch_bounds__(kWriteThreads)
 reshape_and_cache_kernel(const uint4 *__restrict__ key, const uint4 *__restrict__ value,
                          uint4 *__restrict__ key_cache, uint4 *__restrict__ value_cache,
-                         const int64_t *__restrict__ slot_mapping, int vecs_per_row,
+                         const int64_t *__restrict__ slot_mapping, int vecs_per_row, int num_tokens,
                          int64_t num_slots, int32_t *status) {
     pdl_wait_previous();
     pdl_launch_dependents();
-    const int t = blockIdx.x;
-    const int64_t slot = slot_mapping[t];
-    if (slot < 0) return;  // padding token
-    if (slot >= num_slots) {
-        if (threadIdx.x == 0) report(status, PA_DEVERR_SLOT);
-        return;
-    }
-    const uint4 *ks = key + (int64_t)t * vecs_per_row;
-    const uint4 *vs = value + (int64_t)t * vecs_per_row;
-    uint4 *kd = key_cache + slot * vecs_per_row;
-    uint4 *vd = value_cache + slot * vecs_per_row;
-    for (int i = threadIdx.x; i < vecs_per_row; i += kCopyThreads) {
-        uint4 k = ks[i];
-        uint4 v = vs[i];
-        kd[i] = k;
-        vd[i] = v;
+    const int64_t total = (int64_t)num_tokens * vecs_per_row;
+    const int64_t stride = (int64_t)gridDim.x * kWriteThreads;
+    for (int64_t base = (int64_t)blockIdx.x * kWriteThreads + threadIdx.x; base < total;
+         base += stride * kWriteUnroll) {
+        uint4 k[kWriteUnroll], v[kWriteUnroll];
+        int64_t slot[kWriteUnroll];
+        int col[kWriteUnroll];
+#pragma unroll
+        for (int u = 0; u < kWriteUnroll; ++u) {
+            const int64_t i = base + u * stride;
+            if (i < total) {
+                const int64_t t = i / vecs_per_row;
+                col[u] = (int)(i - t * vecs_per_row);
+                slot[u] = slot_mapping[t];
+                k[u] = ldg_stream(key + i);
+                v[u] = ldg_stream(value + i);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kWriteUnroll; ++u) {
+            const int64_t i = base + u * stride;
+            if (i >= total || slot[u] < 0) continue;  // past the end, or a padding token
+            if (slot[u] >= num_slots) {
+                if (col[u] == 0) report(status, PA_DEVERR_SLOT);
+                continue;
+            }
+            key_cache[slot[u] * vecs_per_row + col[u]] = k[u];
+            value_cache[slot[u] * vecs_per_row + col[u]] = v[u];
+        }
     }
 }
 
@@ -118,22 +137,30 @@ reshape_and_cache_rope_kernel(const uint4 *__restrict__ key, const uint4 *__rest
     pdl_wait_previous();
     pdl_launch_dependents();
     const int t = blockIdx.x;
+    const uint4 *ks = key + (int64_t)t * vecs_per_row;
+    const uint4 *vs = value + (int64_t)t * vecs_per_row;
+    // the first vectors of the rows, the slot and the position are loaded together (the
+    // row loads depend on neither)
     const int64_t slot = slot_mapping[t];
+    const int pos = positions[t];
+    uint4 k_first = make_uint4(0, 0, 0, 0), v_first = make_uint4(0, 0, 0, 0);
+    if (threadIdx.x < vecs_per_row) {
+        k_first = ldg_stream(ks + threadIdx.x);
+        v_first = ldg_stream(vs + threadIdx.x);
+    }
     if (slot < 0) return;  // padding token
     if (slot >= num_slots) {
         if (threadIdx.x == 0) report(status, PA_DEVERR_SLOT);
         return;
     }
-    const int pos = positions[t];
     for (int i = threadIdx.x; i < rope_dim / 2; i += kCopyThreads) cs[i] = rope_cos_sin(pos, freqs[i]);
     __syncthreads();
-    const uint4 *ks = key + (int64_t)t * vecs_per_row;
-    const uint4 *vs = value + (int64_t)t * vecs_per_row;
     uint4 *kd = key_cache + slot * vecs_per_row;
     uint4 *vd = value_cache + slot * vecs_per_row;
     for (int i = threadIdx.x; i < vecs_per_row; i += kCopyThreads) {
         const int d0 = (i * EPV) % head_dim;  // first element of the vector within its head
-        uint4 k = ks[i];
+        uint4 k = i < kCopyThreads ? k_first : ks[i];
+        const uint4 vv = i < kCopyThreads ? v_first : vs[i];
         if (d0 < rope_dim) {
             float f[EPV];
             widen(T{}, k, f);
@@ -150,7 +177,7 @@ reshape_and_cache_rope_kernel(const uint4 *__restrict__ key, const uint4 *__rest
             k = narrow16<T>(f);
         }
         kd[i] = k;
-        vd[i] = vs[i];
+        vd[i] = vv;
     }
 }
 
@@ -192,11 +219,17 @@ int launch_reshape_and_cache(const void *key, const void *value, void *key_cache
                              int row_bytes, int block_size, int num_blocks, int32_t *status,
                              cudaStream_t stream) {
     if (num_tokens == 0) return PA_OK;
+    const int vecs = row_bytes / 16;
+    const int64_t total = (int64_t)num_tokens * vecs;
+    const int64_t per_cta = (int64_t)kWriteThreads * kWriteUnroll;
+    const int64_t ctas = (total + per_cta - 1) / per_cta;
+    const int sms = device_sm_count();
+    const int64_t cap = (int64_t)(sms > 0 ? sms : 1) * 8;  // 8 CTAs per SM are resident at once
     const cudaError_t e = launch_pdl(
-        reshape_and_cache_kernel, dim3(num_tokens), dim3(kCopyThreads), 0, stream,
+        reshape_and_cache_kernel, dim3((unsigned)(ctas < cap ? ctas : cap)), dim3(kWriteThreads), 0, stream,
         static_cast<const uint4 *>(key), static_cast<const uint4 *>(value),
         static_cast<uint4 *>(key_cache), static_cast<uint4 *>(value_cache), slot_mapping,
-        row_bytes / 16, (int64_t)num_blocks * block_size, status);
+        vecs, num_tokens, (int64_t)num_blocks * block_size, status);
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 

@@ -10,6 +10,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <utility>
 
 #include "../../include/pa.h"
@@ -149,6 +150,35 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
     cfg.numAttrs = 1;
     cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
     return e == cudaSuccess ? cudaGetLastError() : e;
+}
+
+// Devices a process can address in the per-device tables below.
+constexpr int kMaxDevices = 64;
+
+// launch_pdl for a kernel that needs more than 48 KB of dynamic shared memory.  The limit
+// is raised (cudaFuncSetAttribute) once per device; `ready` is the kernel's own per-device
+// table of flags (static storage, zero at start).  Host threads may race through this:
+// the flags are atomic and raising the limit twice is harmless.  If a launch still fails
+// after the flag was set (the attribute was lost, for instance after cudaDeviceReset),
+// the limit is raised again and the launch retried once.
+template <class... KArgs, class... Args>
+cudaError_t launch_pdl_smem(void (*kernel)(KArgs...), std::atomic<int> *ready, dim3 grid, dim3 block,
+                            size_t smem, cudaStream_t stream, const Args &...args) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::atomic<int> *flag = (dev >= 0 && dev < kMaxDevices) ? &ready[dev] : nullptr;
+    for (int attempt = 0;; ++attempt) {
+        const bool was_set = flag && flag->load(std::memory_order_acquire);
+        if (!was_set) {
+            e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            if (e != cudaSuccess) return e;
+            if (flag) flag->store(1, std::memory_order_release);
+        }
+        e = launch_pdl(kernel, grid, block, smem, stream, args...);
+        if (e == cudaSuccess || !was_set || attempt > 0) return e;
+        flag->store(0, std::memory_order_release);
+    }
 }
 
 }  // namespace pa

@@ -804,22 +804,14 @@ __global__ void __launch_bounds__(D / 2) decode_reduce_kernel(const DecodeParams
 template <class T, int D, int G, bool ROPE>
 int launch_typed(DecodeParams prm, const CUtensorMap &km, const CUtensorMap &vm, cudaStream_t st) {
     using Sh = DecodeShape<T, D, G>;
-    static int configured_device = -1;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (configured_device != dev) {
-        if (cudaFuncSetAttribute(decode_split_kernel<T, D, G, ROPE>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::SMEM) != cudaSuccess)
-            return PA_ERR_CUDA;
-        configured_device = dev;
-    }
+    static std::atomic<int> smem_ready[kMaxDevices];  // per device: shared-memory limit raised
     prm.unit_tokens = Sh::NT * (kConsumerWarps / prm.heads_per_group);
     prm.box_rows = prm.block_size < prm.unit_tokens ? prm.block_size : prm.unit_tokens;
     const bool fused = prm.num_groups * prm.num_seqs < kSegSmem;  // scan inside the split kernel
     if ((!fused &&
          launch_pdl(decode_plan_kernel, dim3(1), dim3(kPlanThreads), 0, st, prm) != cudaSuccess) ||
-        launch_pdl(decode_split_kernel<T, D, G, ROPE>, dim3(prm.grid), dim3(kDecodeThreads), Sh::SMEM, st,
-                   km, vm, prm) != cudaSuccess ||
+        launch_pdl_smem(decode_split_kernel<T, D, G, ROPE>, smem_ready, dim3(prm.grid), dim3(kDecodeThreads),
+                        Sh::SMEM, st, km, vm, prm) != cudaSuccess ||
         launch_pdl(decode_reduce_kernel<D>, dim3(prm.num_groups * prm.num_seqs, prm.heads_per_group * G),
                    dim3(D / 2), 0, st, prm, prm.heads_per_group * G) != cudaSuccess)
         return PA_ERR_CUDA;

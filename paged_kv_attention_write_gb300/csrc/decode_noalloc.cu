@@ -10,11 +10,9 @@
 //
 // The array is a file-scope __device__ variable: every GPU that loads the
 // library holds kNoAllocScratchBytes of it until the process exits.  In host
-// code its name is only a stand-in for the device variable, so its device
-// address is looked up once per device with cudaGetSymbolAddress and that
-// address is what the kernels receive.
-#include <mutex>
-
+// code its name is only a stand-in for the device variable, so every call looks
+// up its device address with cudaGetSymbolAddress in the current context, and
+// that address is what the kernels receive.
 #include "common.cuh"
 
 namespace {
@@ -24,21 +22,16 @@ static_assert(kNoAllocScratchBytes == PA_DECODE_NOALLOC_SCRATCH_BYTES, "header a
 
 static __device__ __align__(256) unsigned char g_decode_scratch[kNoAllocScratchBytes];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_scratch_mutex;
-void *g_scratch_ptr[kMaxDevices];  // device address of g_decode_scratch, per device
-
-// Device address of the scratch array on the current device (resolved on first use).
-int scratch_for_current_device(void **out) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PA_ERR_CUDA;
-    std::lock_guard<std::mutex> lock(g_scratch_mutex);
-    if (!g_scratch_ptr[dev]) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || !p) return PA_ERR_CUDA;
-        g_scratch_ptr[dev] = p;
-    }
-    *out = g_scratch_ptr[dev];
+// Device address of the scratch array in the current context.  The address belongs to
+// the context's copy of the library's device code, not to the device ordinal: a value
+// kept from an earlier call would be stale after cudaDeviceReset, or when the caller
+// switches between several contexts on one device, so it is looked up on every call.
+// The first lookup in a context loads the library's device code there; later ones are a
+// host-side table read.
+int scratch_for_current_context(void **out) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || !p) return PA_ERR_CUDA;
+    *out = p;
     return PA_OK;
 }
 
@@ -60,7 +53,7 @@ extern "C" int pa_decode_noalloc(void *out, pa_dtype out_dtype, const void *quer
     if (need > kNoAllocScratchBytes) return PA_ERR_WORKSPACE;
     void *scratch = nullptr;
     if (need > 0) {
-        const int rc = scratch_for_current_device(&scratch);
+        const int rc = scratch_for_current_context(&scratch);
         if (rc != PA_OK) return rc;
     }
     // Every scratch entry the kernels read is written earlier in the same call, so

@@ -824,15 +824,7 @@ int launch_typed(const PrefillParams &prm, const CUtensorMap &qm, const CUtensor
                  const CUtensorMap &vm, int max_query_len, int num_seqs, cudaStream_t st) {
     constexpr int TT = kBM / G;
     const int smem = PfShape<D>::SMEM;
-    static int configured_device = -1;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (configured_device != dev) {
-        if (cudaFuncSetAttribute(prefill_tc_kernel<T, D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 smem) != cudaSuccess)
-            return PA_ERR_CUDA;
-        configured_device = dev;
-    }
+    static std::atomic<int> smem_ready[kMaxDevices];  // per device: shared-memory limit raised
     PrefillParams p = prm;
     p.q_tiles = (max_query_len + TT - 1) / TT;
     const int64_t items = (int64_t)p.q_tiles * num_seqs * prm.num_kv_heads;
@@ -841,8 +833,8 @@ int launch_typed(const PrefillParams &prm, const CUtensorMap &qm, const CUtensor
     // one persistent CTA per SM (the shared memory allows one)
     const int sms = device_sm_count();
     const int grid = (int)std::min<int64_t>(items, sms > 0 ? sms : 1);
-    return launch_pdl(prefill_tc_kernel<T, D, G>, dim3(grid), dim3(kPfThreads), smem, st, qm, km, vm, p) ==
-                   cudaSuccess
+    return launch_pdl_smem(prefill_tc_kernel<T, D, G>, smem_ready, dim3(grid), dim3(kPfThreads), smem, st, qm,
+                           km, vm, p) == cudaSuccess
                ? PA_OK
                : PA_ERR_CUDA;
 }

@@ -5,6 +5,7 @@ input generator, the host-side argument checks of the C-ABI library and the
 multi-rank host logic.  ``-m gpu`` runs the CUDA parity tests through the
 C-ABI on one GPU.
 """
+import json
 import os
 import sys
 
@@ -39,3 +40,13 @@ def cuda_ok():
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     return True
+
+
+def pytest_sessionfinish(session, exitstatus):
+    """With PA_PARITY_LOG set, write every attention comparison's max-abs / mean-abs."""
+    path = os.environ.get("PA_PARITY_LOG")
+    mod = sys.modules.get("paged_steps")
+    if not path or mod is None or not mod.RECORDS:
+        return
+    with open(path, "w") as f:
+        json.dump(mod.RECORDS, f, indent=0)

@@ -9,11 +9,18 @@ match bit for bit.
 """
 from __future__ import annotations
 
+import os
+
 import numpy as np
 import torch
 
 MAX_ABS = 5e-3
 MEAN_ABS = 5e-4
+
+# (test id, max-abs, mean-abs) of every attention comparison of the session; conftest
+# writes them to the JSON file named by PA_PARITY_LOG at the end of the session, so the
+# margin of each case against the tolerance can be followed from run to run.
+RECORDS: list = []
 
 
 def bits(t: torch.Tensor) -> torch.Tensor:
@@ -71,8 +78,15 @@ def attention_errors(got: torch.Tensor, ref: np.ndarray):
     return float(d.max()), float(d.mean())
 
 
+def record_errors(mx: float, mn: float, max_abs=MAX_ABS, mean_abs=MEAN_ABS):
+    test = os.environ.get("PYTEST_CURRENT_TEST", "?").split(" ")[0]
+    RECORDS.append({"test": test, "max_abs": mx, "mean_abs": mn, "max_abs_bound": max_abs,
+                    "mean_abs_bound": mean_abs})
+
+
 def assert_attention_close(got, ref, max_abs=MAX_ABS, mean_abs=MEAN_ABS):
     mx, mn = attention_errors(got, ref)
+    record_errors(mx, mn, max_abs, mean_abs)
     assert mx <= max_abs and mn <= mean_abs, f"max-abs {mx:.3e} (<= {max_abs}), mean-abs {mn:.3e} (<= {mean_abs})"
     return mx, mn
 

@@ -103,6 +103,49 @@ def test_decode_is_deterministic_and_placement_independent(oracle_mod):
     assert torch.equal(bits(o1), bits(o3))
 
 
+def _decode_subset(case, t, seqs):
+    """pa_decode of the sequences `seqs` of an already written case (shared pools)."""
+    import paged_kv_attention_write_gb300 as pa
+    idx = torch.tensor(seqs, dtype=torch.int64, device="cuda")
+    q, bt, cl = t["q"][idx].contiguous(), t["bt"][idx].contiguous(), t["cl"][idx].contiguous()
+    mcl = int(case.context_lens[seqs].max())
+    out = torch.full(tuple(q.shape), float("nan"), dtype=torch.float32, device="cuda")
+    n = pa.pa_decode_workspace_size(len(seqs), case.num_heads, case.num_kv_heads, case.head_dim, mcl)
+    ws = torch.empty(n, dtype=torch.uint8, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pa.pa_decode(out, q, t["kc"], t["vc"], bt, cl, mcl, case.scale, workspace=ws, status=status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    return out.cpu()
+
+
+def test_decode_result_independent_of_split(oracle_mod):
+    """The same long sequence decoded alone and inside batches of different sizes: the
+    balanced split cuts it into about 152, 40 and 10 pieces at different boundaries (the
+    split follows every sequence's length), and its rows agree within 1e-5 each time; every
+    batch also matches the oracle."""
+    import paged_kv_attention_write_gb300 as pa
+    rng = np.random.default_rng(17)
+    lens = [30000] + [int(x) for x in rng.integers(6000, 14000, size=7)] + \
+           [int(x) for x in rng.integers(100, 3000, size=56)]
+    case = workloads.make_decode_case("split", lens, 32, 32, 8, 128, torch.bfloat16, 17)
+    t = {"q": case.query.cuda(), "kc": case.key_cache.cuda(), "vc": case.value_cache.cuda(),
+         "bt": case.block_tables.cuda(), "cl": case.context_lens.cuda()}
+    pa.pa_reshape_and_cache(case.new_key.cuda(), case.new_value.cuda(), t["kc"], t["vc"],
+                            case.slot_mapping.cuda())
+    _, okc, ovc = oracle_step(case, oracle_mod)
+    rows = []
+    for seqs in ([0], list(range(8)), list(range(64))):
+        out = _decode_subset(case, t, seqs)
+        qsl = torch.arange(len(seqs) + 1, dtype=torch.int32)
+        ref = oracle_mod.paged_attention(case.query[seqs], qsl, okc, ovc, case.block_tables[seqs],
+                                         case.context_lens[seqs], case.scale)
+        assert_attention_close(out, ref)
+        rows.append(out[0])
+    for r in rows[1:]:
+        assert (r - rows[0]).abs().max().item() <= 1e-5
+
+
 @pytest.mark.parametrize("out_dtype", [torch.float16, torch.bfloat16])
 def test_decode_low_precision_output_is_rounded_fp32(oracle_mod, out_dtype):
     case = workloads.make_decode_case("o", [100, 1000, 3000], 32, 32, 8, 128, torch.bfloat16, 4)

@@ -4,9 +4,9 @@ device, bindings without an allocator).  Its scratch is a static array inside th
 library, shared by every call.
 
 The test calls the C entry point directly (ctypes) and checks its output against
-pa_decode with a caller workspace, within the parity tolerance, on two calls in a
-row with different problems, so that the first call's leftover scratch cannot leak
-into the second.  This file is collected last so that a run stopping at the first
+pa_decode with a caller workspace and against the fp64 oracle, within the parity
+tolerance, on two calls in a row with different problems, so that the first call's
+leftover scratch cannot leak into the second.  This file is collected last so that a run stopping at the first
 failure has already run every other test; it also passes alone in a fresh process.
 """
 import ctypes
@@ -15,7 +15,7 @@ import pytest
 import torch
 
 import workloads
-from paged_steps import MAX_ABS, MEAN_ABS
+from paged_steps import MAX_ABS, MEAN_ABS, assert_attention_close, oracle_step
 
 pytestmark = pytest.mark.gpu
 
@@ -60,7 +60,7 @@ def _workspace_decode(case, t):
     return out
 
 
-def test_noalloc_matches_workspace_decode_on_two_calls_in_a_row():
+def test_noalloc_matches_workspace_decode_on_two_calls_in_a_row(oracle_mod):
     import paged_kv_attention_write_gb300 as pa
     lib = ctypes.CDLL(str(pa.library_path()))
     cases = [workloads.decode_batch(),
@@ -79,6 +79,8 @@ def test_noalloc_matches_workspace_decode_on_two_calls_in_a_row():
         d = (out - ref).abs()
         assert torch.isfinite(out).all()
         assert d.max().item() <= MAX_ABS and d.mean().item() <= MEAN_ABS
+        oracle_ref, _, _ = oracle_step(case, oracle_mod)
+        assert_attention_close(out.cpu(), oracle_ref)
 
 
 def test_noalloc_rejects_problems_beyond_its_scratch():
