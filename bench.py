@@ -593,8 +593,8 @@ def manager_measurement():
 
 SERVE_REPLAY = ("256 requests at once: 70 % start with one of 4 system prompts (128-1024 tokens), "
                 "own text 64-1024 tokens, 32-256 generated tokens; 32 q / 8 kv heads, D 128, bs 16, bf16; "
-                "budget 4096 tokens, 512-token chunks, <= 8 decode steps in a row; q/k/v gathered from "
-                "seeded random tables by (token, position); one device read of each step's output")
+                "budget 4096 tokens, 512-token chunks, <= 8 decode steps in a row; q/k/v gathered on the "
+                "device from seeded random tables by (token, position); one device read of each step's output")
 
 
 def _serve_replay(device, num_requests: int, seed: int):
@@ -614,8 +614,10 @@ def _serve_replay(device, num_requests: int, seed: int):
     gpu = []
 
     def qkv(step):
-        ids = (step["token_ids"].astype(np.int64) * 7919 + step["positions"].astype(np.int64) * 104729) % R
-        i = torch.from_numpy(ids).to(device, non_blocking=True)
+        # the table row of each (token, position), from the step's device copy of both
+        # (int32 arithmetic: token < 32000 and position < 8192 keep the sum below 2^31)
+        tok, pos = eng.device_tokens(step)
+        i = torch.remainder(tok * 7919 + pos * 104729, R)
         e = torch.cuda.Event(enable_timing=True)
         e.record()
         gpu.append([e, None])

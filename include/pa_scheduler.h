@@ -80,6 +80,31 @@ int pa_sched_step(pa_sched *s, pa_sched_batch *batch, int64_t *req_ids, int32_t 
                   int32_t *token_ids, int32_t *positions, int64_t *slot_mapping, int64_t *copy_pairs,
                   int max_seqs, int max_tokens, int max_pairs);
 
+/* Byte offsets of one step's arrays inside the caller's buffer (pa_sched_step_packed).  The
+ * arrays the kernels and the model read come first, in one span of dev_bytes bytes (one
+ * host-to-device copy): query_start_loc, context_lens, block_tables, slot_mapping,
+ * copy_pairs, token_ids, positions; req_ids (host only) follows.  Every array starts on a
+ * 16-byte boundary of the buffer and has the element type and length pa_sched_step gives
+ * it (block-table rows table_width entries apart). */
+typedef struct {
+    int64_t query_start_loc, context_lens, block_tables, slot_mapping, copy_pairs, token_ids, positions;
+    int64_t dev_bytes;
+    int64_t req_ids;
+    int64_t total_bytes;
+} pa_sched_offsets;
+
+/* Buffer bytes pa_sched_step_packed may need for any step with the requests queued so far
+ * (grows when requests are added). */
+int64_t pa_sched_packed_bytes(const pa_sched *s);
+
+/* pa_sched_step with every array of the step written into one caller buffer (host memory,
+ * 16-byte aligned, for instance pinned so that its device span goes over in one asynchronous
+ * copy), laid out for the batch's own sizes as *offsets states.  PA_ERR_WORKSPACE when
+ * buf_bytes < pa_sched_packed_bytes(s) (nothing changes); pa_sched_complete follows as for
+ * pa_sched_step. */
+int pa_sched_step_packed(pa_sched *s, pa_sched_batch *batch, void *buf, int64_t buf_bytes,
+                         pa_sched_offsets *offsets);
+
 /* Finish the planned step with one sampled token per batch sequence (a prefill chunk that is
  * not its prompt's last ignores its entry).  Writes the requests that finished (and were
  * freed) to finished (capacity max_finished, count *num_finished). */

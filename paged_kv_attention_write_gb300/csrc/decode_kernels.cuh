@@ -507,13 +507,45 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
             l_lane[u] = 0.f;
         }
     };
-    auto load_q = [&](int s, int hg, int ctx) {
+    // This lane's 16-byte slices of the G query rows of (sequence s, head group hg).
+    auto q_global = [&](int s, int hg, uint4 (&raw)[G]) {
         const typename T::storage *qp = static_cast<const typename T::storage *>(p.query) +
                                         ((int64_t)s * p.num_heads + hg * HGq + h * G) * D + r * EPV;
+#pragma unroll
+        for (int hh = 0; hh < G; ++hh) raw[hh] = *reinterpret_cast<const uint4 *>(qp + hh * D);
+    };
+    // Query prefetch for the next segment of the range: with eight kv heads per group (the
+    // flush then needs no shared memory) each warp copies its rows into its own slice of
+    // red_o with cp.async while it streams the segment's last unit, so that the switch
+    // waits for no global load.
+    const bool q_prefetch = G <= 4 && HG == NW;
+    const uint32_t q_slot = smem_u32(red_o) + (uint32_t)(warp * G * D * (int)sizeof(typename T::storage));
+    auto q_prefetch_issue = [&](int s, int hg) {
+        if (grp == 0) {
+            const typename T::storage *qp = static_cast<const typename T::storage *>(p.query) +
+                                            ((int64_t)s * p.num_heads + hg * HGq + h * G) * D + r * EPV;
+#pragma unroll
+            for (int hh = 0; hh < G; ++hh)
+                asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                                 q_slot + (uint32_t)((hh * D + r * EPV) * (int)sizeof(typename T::storage))),
+                             "l"(qp + hh * D)
+                             : "memory");
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+    auto q_prefetched = [&](uint4 (&raw)[G]) {
+        asm volatile("cp.async.wait_all;" ::: "memory");
+        __syncwarp();
+#pragma unroll
+        for (int hh = 0; hh < G; ++hh)
+            raw[hh] = lds128(q_slot + (uint32_t)((hh * D + r * EPV) * (int)sizeof(typename T::storage)));
+        __syncwarp();  // every lane has read the slice before the next prefetch overwrites it
+    };
+    auto load_q = [&](const uint4 (&qraw)[G], int ctx) {
         if constexpr (!ROPE) {
 #pragma unroll
             for (int hh = 0; hh < G; ++hh) {
-                const uint4 raw = *reinterpret_cast<const uint4 *>(qp + hh * D);
+                const uint4 raw = qraw[hh];
                 widen_vec<T>(raw, q2[hh]);
 #pragma unroll
                 for (int e = 0; e < EPV / 2; ++e) {
@@ -524,7 +556,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
         } else {
 #pragma unroll
             for (int hh = 0; hh < G; ++hh) {
-                const uint4 raw = *reinterpret_cast<const uint4 *>(qp + hh * D);
+                const uint4 raw = qraw[hh];
                 widen_vec<T>(raw, q2[hh]);
             }
             // RoPE at the newest token's position (GPT-J pairs: this lane's float2 entries
@@ -664,6 +696,33 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
             for (int o = 1; o < 32; o <<= 1) v += __shfl_xor_sync(kFullMask, v, o);
             lsum[hh] = v;
         }
+        const int s = k % S, hg = k / S, nsub = NW / HG;
+        if (G <= 4 && nsub == 1) {  // every warp holds whole rows of its kv head: write from registers
+            if (grp == 0) {
+#pragma unroll
+                for (int hh = 0; hh < G; ++hh) {
+                    const int hl = h * G + hh;
+                    if (whole) {
+                        const float inv = 1.f / lsum[hh];
+                        const int64_t o0 = ((int64_t)s * p.num_heads + hg * HGq + hl) * D + r * EPV;
+#pragma unroll
+                        for (int e = 0; e < EPV / 2; ++e)
+                            store_pair_any(p.out, p.out_dtype, o0 + 2 * e, acc[hh][e].x * inv, acc[hh][e].y * inv);
+                    } else {
+                        const int64_t pi = (int64_t)(c + k) * HGq + hl;
+#pragma unroll
+                        for (int e = 0; e < EPV / 2; ++e)
+                            *reinterpret_cast<float2 *>(p.part_o + pi * D + r * EPV + 2 * e) = acc[hh][e];
+                        if (r == 0) {
+                            p.part_m[pi] = m[hh];
+                            p.part_l[pi] = lsum[hh];
+                        }
+                    }
+                }
+            }
+            reset();
+            return;
+        }
         if (grp == 0) {
 #pragma unroll
             for (int hh = 0; hh < G; ++hh)
@@ -679,7 +738,6 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
             }
         }
         named_barrier(1, NW * 32);
-        const int s = k % S, hg = k / S, nsub = NW / HG;
         for (int idx = threadIdx.x; idx < HGq * (D / 2); idx += NW * 32) {
             const int hl = idx / (D / 2), d = (idx % (D / 2)) * 2;
             const int hk = hl / G, hh = hl % G;
@@ -713,7 +771,13 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
     reset();
     int k = k0, seg_beg = segs[k], seg_end = segs[k + 1];
     int s = k % S, hg = k / S, ctx = context_of(s);
-    load_q(s, hg, ctx);
+    {
+        uint4 raw[G];
+        q_global(s, hg, raw);
+        load_q(raw, ctx);
+    }
+    bool pf_pending = false;
+    int pf_ctx = 0;
     for (int u = u0, i = 0; u < u1; ++u, ++i) {
         if (u >= seg_end) {
             while (u >= seg_end) {
@@ -723,8 +787,23 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
             }
             s = k % S;
             hg = k / S;
-            ctx = context_of(s);
-            load_q(s, hg, ctx);
+            uint4 raw[G];
+            if (pf_pending) {
+                q_prefetched(raw);
+                ctx = pf_ctx;
+                pf_pending = false;
+            } else {
+                ctx = context_of(s);
+                q_global(s, hg, raw);
+            }
+            load_q(raw, ctx);
+        }
+        if (q_prefetch && u + 1 == seg_end && u + 1 < u1) {  // the next unit starts a segment
+            int kn = k + 1;
+            while (segs[kn + 1] <= u + 1) ++kn;  // skip segments with nothing to attend
+            q_prefetch_issue(kn % S, kn / S);
+            pf_ctx = context_of(kn % S);
+            pf_pending = true;
         }
         const int stage = i % NSTAGE;
         const uint32_t parity = (i / NSTAGE) & 1;
@@ -750,14 +829,18 @@ constexpr int kMaxPieces = 1024;  // CTAs of the split kernel (one per SM)
 constexpr int kReduceBatch = 32;  // pieces whose loads are in flight together
 
 // For every segment split over several CTAs: out = sum_c 2^(m_c - M) acc_c /
-// sum_c 2^(m_c - M) l_c.  grid = (segment, query head of the group); one thread
-// per pair of outputs.  The loads of a batch of pieces are all issued before any
-// is used (two memory round trips for the usual segment of < 32 pieces), and the
+// sum_c 2^(m_c - M) l_c.  grid = (segment, group of blockDim.y query heads of the
+// group); one thread per pair of outputs of one head.  The launcher packs up to
+// kReduceHeads heads per CTA while that still leaves about a wave of CTAs, so that few
+// small CTAs have to be scheduled after the split kernel.  The loads of a batch of pieces are all issued before
+// any is used (two memory round trips for the usual segment of < 32 pieces), and the
 // batch is merged online (running max).
+constexpr int kReduceHeads = 8;
 template <int D>
-__global__ void __launch_bounds__(D / 2) decode_reduce_kernel(const DecodeParams p, int HGq) {
+__global__ void __launch_bounds__(D / 2 * kReduceHeads) decode_reduce_kernel(const DecodeParams p, int HGq) {
     pdl_wait_previous();
-    const int k = blockIdx.x, hl = blockIdx.y, d = threadIdx.x * 2;
+    const int k = blockIdx.x, hl = blockIdx.y * blockDim.y + threadIdx.y, d = threadIdx.x * 2;
+    if (hl >= HGq) return;
     const int S = p.num_seqs, K = p.num_groups * S;
     const int N = p.seg_start[K];
     const int beg = p.seg_start[k], end = p.seg_start[k + 1];
@@ -808,12 +891,16 @@ int launch_typed(DecodeParams prm, const CUtensorMap &km, const CUtensorMap &vm,
     prm.unit_tokens = Sh::NT * (kConsumerWarps / prm.heads_per_group);
     prm.box_rows = prm.block_size < prm.unit_tokens ? prm.block_size : prm.unit_tokens;
     const bool fused = prm.num_groups * prm.num_seqs < kSegSmem;  // scan inside the split kernel
+    // reduce: heads per CTA, as many as keep about 128 CTAs (one wave)
+    const int K = prm.num_groups * prm.num_seqs, HGq = prm.heads_per_group * G;
+    int rh = kReduceHeads;
+    while (rh > 1 && (int64_t)K * ((HGq + rh - 1) / rh) < 128) rh >>= 1;
     if ((!fused &&
          launch_pdl(decode_plan_kernel, dim3(1), dim3(kPlanThreads), 0, st, prm) != cudaSuccess) ||
         launch_pdl_smem(decode_split_kernel<T, D, G, ROPE>, smem_ready, dim3(prm.grid), dim3(kDecodeThreads),
                         Sh::SMEM, st, km, vm, prm) != cudaSuccess ||
-        launch_pdl(decode_reduce_kernel<D>, dim3(prm.num_groups * prm.num_seqs, prm.heads_per_group * G),
-                   dim3(D / 2), 0, st, prm, prm.heads_per_group * G) != cudaSuccess)
+        launch_pdl(decode_reduce_kernel<D>, dim3(K, (HGq + rh - 1) / rh), dim3(D / 2, rh), 0, st, prm, HGq) !=
+            cudaSuccess)
         return PA_ERR_CUDA;
     return PA_OK;
 }

@@ -180,18 +180,12 @@ int pa_sched_capacity(const pa_sched *s, int out[4]) {
     return PA_OK;
 }
 
-int pa_sched_step(pa_sched *s, pa_sched_batch *b, int64_t *req_ids, int32_t *query_start_loc,
-                  int32_t *context_lens, int32_t *block_tables, int table_capacity,
-                  int32_t *token_ids, int32_t *positions, int64_t *slot_mapping, int64_t *copy_pairs,
-                  int max_seqs, int max_tokens, int max_pairs) {
-    if (!s || !b || s->planned) return PA_ERR_INVALID_ARG;
-    int cap[4];
-    pa_sched_capacity(s, cap);
-    if (max_seqs < cap[0] || max_tokens < cap[1] || table_capacity < cap[2] || max_pairs < cap[3])
-        return PA_ERR_WORKSPACE;
-    if (!req_ids || !query_start_loc || !context_lens || !block_tables || !token_ids || !positions ||
-        !slot_mapping || !copy_pairs)
-        return PA_ERR_INVALID_ARG;
+}  // extern "C"
+
+namespace {
+
+// Plans the next step (sets the batch entries, the copy pairs and the kind).
+void plan_step(pa_sched *s) {
     s->last.clear();
     s->pairs.clear();
     s->last_kind = PA_SCHED_IDLE;
@@ -204,14 +198,32 @@ int pa_sched_step(pa_sched *s, pa_sched_batch *b, int64_t *req_ids, int32_t *que
         s->decode_batch();
         s->last_kind = PA_SCHED_DECODE;
     }
-    // describe the batch
+}
+
+// Sizes of the planned batch.
+void describe(const pa_sched *s, pa_sched_batch *b) {
     int width = 1, tokens = 0, max_q = 0, max_c = 0;
     for (const Entry &e : s->last) {
         const auto &bl = s->kv->reqs.at(e.rid).blocks;
         width = std::max(width, (int)bl.size());
         max_q = std::max(max_q, e.count);
         max_c = std::max(max_c, e.start + e.count);
+        tokens += e.count;
     }
+    b->kind = s->last_kind;
+    b->num_seqs = (int)s->last.size();
+    b->num_tokens = tokens;
+    b->max_query_len = max_q;
+    b->max_context_len = max_c;
+    b->table_width = width;
+    b->num_copy_pairs = (int)s->pairs.size() / 2;
+}
+
+// Writes the planned batch's arrays (block-table rows table_width entries apart).
+void write_batch(const pa_sched *s, int table_width, int64_t *req_ids, int32_t *query_start_loc,
+                 int32_t *context_lens, int32_t *block_tables, int32_t *token_ids, int32_t *positions,
+                 int64_t *slot_mapping, int64_t *copy_pairs) {
+    int tokens = 0;
     query_start_loc[0] = 0;
     for (size_t i = 0; i < s->last.size(); ++i) {
         const Entry &e = s->last[i];
@@ -219,8 +231,8 @@ int pa_sched_step(pa_sched *s, pa_sched_batch *b, int64_t *req_ids, int32_t *que
         const SReq &r = s->req.at(e.rid);
         req_ids[i] = e.rid;
         context_lens[i] = e.start + e.count;
-        int32_t *row = block_tables + i * (size_t)width;
-        for (int j = 0; j < width; ++j) row[j] = j < (int)bl.size() ? bl[j] : 0;
+        int32_t *row = block_tables + i * (size_t)table_width;
+        for (int j = 0; j < table_width; ++j) row[j] = j < (int)bl.size() ? bl[j] : 0;
         for (int p = e.start; p < e.start + e.count; ++p, ++tokens) {
             token_ids[tokens] = r.tokens[p];
             positions[tokens] = p;
@@ -229,13 +241,72 @@ int pa_sched_step(pa_sched *s, pa_sched_batch *b, int64_t *req_ids, int32_t *que
         query_start_loc[i + 1] = tokens;
     }
     for (size_t i = 0; i < s->pairs.size(); ++i) copy_pairs[i] = s->pairs[i];
-    b->kind = s->last_kind;
-    b->num_seqs = (int)s->last.size();
-    b->num_tokens = tokens;
-    b->max_query_len = max_q;
-    b->max_context_len = max_c;
-    b->table_width = width;
-    b->num_copy_pairs = (int)s->pairs.size() / 2;
+}
+
+int64_t round16(int64_t x) { return (x + 15) & ~int64_t(15); }
+
+// Byte layout of a packed step with S sequences, T tokens, table rows of W entries and P
+// copy pairs (the device span first).
+pa_sched_offsets packed_layout(int64_t S, int64_t T, int64_t W, int64_t P) {
+    pa_sched_offsets o{};
+    int64_t at = 0;
+    o.query_start_loc = at; at += round16(4 * (S + 1));
+    o.context_lens = at;    at += round16(4 * S);
+    o.block_tables = at;    at += round16(4 * S * W);
+    o.slot_mapping = at;    at += round16(8 * T);
+    o.copy_pairs = at;      at += round16(16 * P);
+    o.token_ids = at;       at += round16(4 * T);
+    o.positions = at;       at += round16(4 * T);
+    o.dev_bytes = at;
+    o.req_ids = at;         at += round16(8 * S);
+    o.total_bytes = at;
+    return o;
+}
+
+}  // namespace
+
+extern "C" {
+
+int pa_sched_step(pa_sched *s, pa_sched_batch *b, int64_t *req_ids, int32_t *query_start_loc,
+                  int32_t *context_lens, int32_t *block_tables, int table_capacity,
+                  int32_t *token_ids, int32_t *positions, int64_t *slot_mapping, int64_t *copy_pairs,
+                  int max_seqs, int max_tokens, int max_pairs) {
+    if (!s || !b || s->planned) return PA_ERR_INVALID_ARG;
+    int cap[4];
+    pa_sched_capacity(s, cap);
+    if (max_seqs < cap[0] || max_tokens < cap[1] || table_capacity < cap[2] || max_pairs < cap[3])
+        return PA_ERR_WORKSPACE;
+    if (!req_ids || !query_start_loc || !context_lens || !block_tables || !token_ids || !positions ||
+        !slot_mapping || !copy_pairs)
+        return PA_ERR_INVALID_ARG;
+    plan_step(s);
+    describe(s, b);
+    write_batch(s, b->table_width, req_ids, query_start_loc, context_lens, block_tables, token_ids, positions,
+                slot_mapping, copy_pairs);
+    s->planned = true;
+    return PA_OK;
+}
+
+int64_t pa_sched_packed_bytes(const pa_sched *s) {
+    int cap[4];
+    if (pa_sched_capacity(s, cap) != PA_OK) return 0;
+    return packed_layout(cap[0], cap[1], cap[2], cap[3]).total_bytes;
+}
+
+int pa_sched_step_packed(pa_sched *s, pa_sched_batch *b, void *buf, int64_t buf_bytes, pa_sched_offsets *offsets) {
+    if (!s || !b || !buf || !offsets || s->planned || (reinterpret_cast<uintptr_t>(buf) & 15))
+        return PA_ERR_INVALID_ARG;
+    if (buf_bytes < pa_sched_packed_bytes(s)) return PA_ERR_WORKSPACE;
+    plan_step(s);
+    describe(s, b);
+    const pa_sched_offsets o = packed_layout(b->num_seqs, b->num_tokens, b->table_width, b->num_copy_pairs);
+    char *base = static_cast<char *>(buf);
+    write_batch(s, b->table_width, reinterpret_cast<int64_t *>(base + o.req_ids),
+                reinterpret_cast<int32_t *>(base + o.query_start_loc), reinterpret_cast<int32_t *>(base + o.context_lens),
+                reinterpret_cast<int32_t *>(base + o.block_tables), reinterpret_cast<int32_t *>(base + o.token_ids),
+                reinterpret_cast<int32_t *>(base + o.positions), reinterpret_cast<int64_t *>(base + o.slot_mapping),
+                reinterpret_cast<int64_t *>(base + o.copy_pairs));
+    *offsets = o;
     s->planned = true;
     return PA_OK;
 }

@@ -1,13 +1,17 @@
 """Step loop over the scheduler and the paged-attention kernels.
 
 ``PagedAttentionEngine`` runs one scheduler step at a time (``include/pa_scheduler.h``:
-prefill or decode batches under a token budget, chunked prompts, prefix caching): it moves
-the step's batch description to the device in one copy, applies copy-on-write block copies,
-writes the batch's fresh K/V into the paged cache and runs decode or chunked-prefill
-attention.  The model side is supplied by the caller: ``qkv(step)`` returns the device
-tensors q ``[T][Hq][D]``, k and v ``[T][Hkv][D]`` of the step's query tokens (``step`` holds
-their token ids and positions), ``sample(step, out)`` returns one next token per sequence.
-Marshalling only: every computation on the data runs in the library's kernels.
+prefill or decode batches under a token budget, chunked prompts, prefix caching).  Per step
+the C++ scheduler writes the whole batch description into one pinned host buffer
+(``pa_sched_step_packed``), its device part goes over in one asynchronous copy
+(``pa_engine_upload``), and one more call (``pa_engine_attend``) enqueues the step's
+copy-on-write block copies, the fresh K/V written into the paged cache and decode or
+chunked-prefill attention, reading the batch from that copy.  The model
+side is supplied by the caller: ``qkv(step)`` returns the device tensors q ``[T][Hq][D]``, k and
+v ``[T][Hkv][D]`` of the step's query tokens (``step`` holds their token ids and positions, on
+the host and, through ``device_tokens``, on the device), ``sample(step, out)`` returns one next
+token per sequence.  Marshalling only: every computation on the data runs in the library's
+kernels.
 """
 from __future__ import annotations
 
@@ -16,10 +20,29 @@ from typing import Callable, Optional
 import numpy as np
 import torch
 
-from . import pa_copy_blocks, pa_decode, pa_decode_workspace_size, pa_prefill_chunk, pa_reshape_and_cache
-from .kv_manager import Scheduler
+import ctypes
+
+from . import _DTYPES, _check, _lib, pa_decode_workspace_size
+from .kv_manager import KIND_NAMES, Scheduler, _Batch, _Offsets
+
+
+class _Cache(ctypes.Structure):
+    _fields_ = [("key_cache", ctypes.c_void_p), ("value_cache", ctypes.c_void_p), ("num_blocks", ctypes.c_int),
+                ("block_size", ctypes.c_int), ("num_heads", ctypes.c_int), ("num_kv_heads", ctypes.c_int),
+                ("head_dim", ctypes.c_int), ("kv_dtype", ctypes.c_int), ("scale", ctypes.c_float)]
+
+
+_lib.pa_engine_upload.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.POINTER(_Offsets), ctypes.c_void_p]
+_lib.pa_engine_upload.restype = ctypes.c_int
+_lib.pa_engine_attend.argtypes = [ctypes.POINTER(_Cache), ctypes.POINTER(_Batch), ctypes.POINTER(_Offsets),
+                                  ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                  ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t,
+                                  ctypes.c_void_p, ctypes.c_void_p]
+_lib.pa_engine_attend.restype = ctypes.c_int
 
 __all__ = ["PagedAttentionEngine"]
+
+_PA_F32 = 0
 
 
 class PagedAttentionEngine:
@@ -31,70 +54,89 @@ class PagedAttentionEngine:
                                prefix_cache)
         self.dev = torch.device(device)
         self.Hq, self.Hkv, self.D, self.bs = num_heads, num_kv_heads, head_dim, block_size
+        self.NB = num_blocks
         self.scale = scale if scale is not None else 1.0 / head_dim ** 0.5
+        self.dtype_code = _DTYPES[dtype]
         self.key_cache = torch.zeros((num_blocks, block_size, num_kv_heads, head_dim), dtype=dtype, device=self.dev)
         self.value_cache = torch.zeros_like(self.key_cache)
-        self._pinned = None
+        self._cache = _Cache(self.key_cache.data_ptr(), self.value_cache.data_ptr(), num_blocks, block_size,
+                             num_heads, num_kv_heads, head_dim, self.dtype_code, self.scale)
+        # two pinned staging buffers used in turn, each with the event of its last copy out
+        self._pinned = [None, None]
+        self._events = [None, None]
+        self._turn = 0
         self._dev_buf = None
-        self._copied = None   # event after the last copy out of the pinned buffer
+        self._out = None
         self._ws = None
 
     def add_request(self, req_id: int, prompt, max_new_tokens: int) -> None:
         self.sched.add_request(req_id, prompt, max_new_tokens)
 
-    def _to_device(self, b: dict):
-        """The step's int arrays in one pinned buffer, one host-to-device copy."""
-        parts = [b["query_start_loc"], b["context_lens"], b["block_tables"].reshape(-1), b["slot_mapping"],
-                 b["copy_pairs"].reshape(-1)]
-        sizes = [p.nbytes for p in parts]
-        need = sum((s + 15) // 16 * 16 for s in sizes)
-        if self._copied is not None:   # the previous step's copy has left the pinned buffer
-            self._copied.synchronize()
-        if self._pinned is None or self._pinned.numel() < need:
-            self._pinned = torch.empty(need * 2, dtype=torch.uint8, pin_memory=True)
-            self._dev_buf = torch.empty(need * 2, dtype=torch.uint8, device=self.dev)
-        host = self._pinned.numpy()
-        offs, o = [], 0
-        for p, s in zip(parts, sizes):
-            host[o:o + s] = p.view(np.uint8).reshape(-1)
-            offs.append(o)
-            o += (s + 15) // 16 * 16
-        self._dev_buf[:o].copy_(self._pinned[:o], non_blocking=True)
-        if self._copied is None:
-            self._copied = torch.cuda.Event()
-        self._copied.record()
-        out = []
-        for p, off, s in zip(parts, offs, sizes):
-            dt = {np.dtype(np.int32): torch.int32, np.dtype(np.int64): torch.int64}[p.dtype]
-            out.append(self._dev_buf[off:off + s].view(dt))
-        return out
+    def _buffers(self):
+        """The next pinned staging buffer (free once its previous copy has left it) and the
+        device buffer, grown to the scheduler's packed size."""
+        need = self.sched.packed_bytes()
+        i = self._turn
+        self._turn ^= 1
+        if self._events[i] is not None:
+            self._events[i].synchronize()
+        if self._pinned[i] is None or self._pinned[i].numel() < need:
+            self._pinned[i] = torch.empty(2 * need, dtype=torch.uint8, pin_memory=True)
+        if self._dev_buf is None or self._dev_buf.numel() < need:
+            self._dev_buf = torch.empty(2 * need, dtype=torch.uint8, device=self.dev)
+        return i
+
+    def device_tokens(self, step: dict):
+        """The step's token ids and positions as int32 device tensors (views of the copy)."""
+        o, T = step["_offsets"], step["num_tokens"]
+        buf = self._dev_buf
+        tok = buf[o.token_ids:o.token_ids + 4 * T].view(torch.int32)
+        pos = buf[o.positions:o.positions + 4 * T].view(torch.int32)
+        return tok, pos
 
     def step(self, qkv: Callable, sample: Callable) -> Optional[dict]:
         """Run one scheduler step; returns the step (batch description and ``out``), or None
-        when the scheduler is idle."""
-        b = self.sched.step()
-        if b["kind"] == "idle":
+        when the scheduler is idle.  The step's host arrays are views of the staging buffer and
+        ``out`` a view of the engine's output buffer: both stay valid until the next step."""
+        i = self._buffers()
+        host = self._pinned[i]
+        b, o = self.sched.step_packed(host.data_ptr(), host.numel())
+        if b.kind == 0:
+            self.sched.complete([])  # close the idle step: requests added later can run
             return None
-        S, W = b["num_seqs"], b["block_tables"].shape[1]
-        qsl, cl, bt, slots, pairs = self._to_device(b)
-        bt = bt.view(S, W)
-        if b["copy_pairs"].size:
-            pa_copy_blocks(self.key_cache, self.value_cache, pairs.view(-1, 2))
-        q, k, v = qkv(b)
-        pa_reshape_and_cache(k, v, self.key_cache, self.value_cache, slots)
-        out = torch.empty((b["num_tokens"], self.Hq, self.D), dtype=torch.float32, device=self.dev)
-        if b["kind"] == "decode":
-            need = max(1, pa_decode_workspace_size(S, self.Hq, self.Hkv, self.D, b["max_context_len"]))
+        S, T = b.num_seqs, b.num_tokens
+        stream = torch.cuda.current_stream().cuda_stream
+        _check(_lib.pa_engine_upload(self._dev_buf.data_ptr(), host.data_ptr(), ctypes.byref(o), stream),
+               "pa_engine_upload")
+        if self._events[i] is None:
+            self._events[i] = torch.cuda.Event()
+        self._events[i].record()
+        hb = host.numpy()
+        step = {"kind": KIND_NAMES[b.kind], "num_seqs": S, "num_tokens": T,
+                "max_query_len": b.max_query_len, "max_context_len": b.max_context_len,
+                "req_ids": np.frombuffer(hb, np.int64, S, o.req_ids),
+                "query_start_loc": np.frombuffer(hb, np.int32, S + 1, o.query_start_loc),
+                "context_lens": np.frombuffer(hb, np.int32, S, o.context_lens),
+                "token_ids": np.frombuffer(hb, np.int32, T, o.token_ids),
+                "positions": np.frombuffer(hb, np.int32, T, o.positions),
+                "_offsets": o}
+        q, k, v = qkv(step)
+        if self._out is None or self._out.shape[0] < T:
+            self._out = torch.empty((max(T, 2 * (0 if self._out is None else self._out.shape[0])), self.Hq, self.D),
+                                    dtype=torch.float32, device=self.dev)
+        out = self._out[:T]
+        ws, ws_bytes = None, 0
+        if b.kind == 2:  # decode: a workspace for the split of the contexts
+            need = max(1, pa_decode_workspace_size(S, self.Hq, self.Hkv, self.D, b.max_context_len))
             if self._ws is None or self._ws.numel() < need:
                 self._ws = torch.empty(need * 2, dtype=torch.uint8, device=self.dev)
-            pa_decode(out, q, self.key_cache, self.value_cache, bt, cl, b["max_context_len"], self.scale,
-                      workspace=self._ws)
-        else:
-            pa_prefill_chunk(out, q, qsl, b["max_query_len"], self.key_cache, self.value_cache, bt, cl,
-                             b["max_context_len"], self.scale)
-        b["out"] = out
-        self.sched.complete(sample(b, out))
-        return b
+            ws, ws_bytes = self._ws.data_ptr(), self._ws.numel()
+        _check(_lib.pa_engine_attend(ctypes.byref(self._cache), ctypes.byref(b), ctypes.byref(o),
+                                     self._dev_buf.data_ptr(), q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                     out.data_ptr(), _PA_F32, ws, ws_bytes, None, stream), "pa_engine_attend")
+        step["out"] = out
+        self.sched.complete(sample(step, out))
+        return step
 
     def run(self, qkv: Callable, sample: Callable, max_steps: int = 10 ** 7) -> int:
         """Steps until idle; returns the number of steps."""

@@ -129,7 +129,17 @@ class _Batch(ctypes.Structure):
                 ("max_context_len", _i32), ("table_width", _i32), ("num_copy_pairs", _i32)]
 
 
+class _Offsets(ctypes.Structure):
+    _fields_ = [(n, _i64) for n in ("query_start_loc", "context_lens", "block_tables", "slot_mapping",
+                                    "copy_pairs", "token_ids", "positions", "dev_bytes", "req_ids",
+                                    "total_bytes")]
+
+
 _lib.pa_sched_create.argtypes = [_i32, _i32, _i32, _i32, _i32, _i32, ctypes.POINTER(_vp)]
+_lib.pa_sched_packed_bytes.argtypes = [_vp]
+_lib.pa_sched_packed_bytes.restype = _i64
+_lib.pa_sched_step_packed.argtypes = [_vp, ctypes.POINTER(_Batch), _vp, _i64, ctypes.POINTER(_Offsets)]
+_lib.pa_sched_step_packed.restype = _i32
 _lib.pa_sched_destroy.argtypes = [_vp]
 _lib.pa_sched_destroy.restype = None
 _lib.pa_sched_add_request.argtypes = [_vp, _i64, _vp, _i32, _i32]
@@ -206,6 +216,19 @@ class Scheduler:
                 "context_lens": b["context_lens"][:S], "block_tables": b["tables"][:S * W].reshape(S, W),
                 "token_ids": b["token_ids"][:T], "positions": b["positions"][:T],
                 "slot_mapping": b["slots"][:T], "copy_pairs": b["pairs"][:2 * out.num_copy_pairs].reshape(-1, 2)}
+
+    def packed_bytes(self) -> int:
+        """Buffer bytes ``step_packed`` may need with the requests queued so far."""
+        return int(_lib.pa_sched_packed_bytes(self._h))
+
+    def step_packed(self, buf_ptr: int, buf_bytes: int):
+        """Plan the next step into one host buffer (``pa_sched_step_packed``); returns the
+        batch sizes and the byte offsets of its arrays (ctypes structures)."""
+        b, o = _Batch(), _Offsets()
+        _check(_lib.pa_sched_step_packed(self._h, ctypes.byref(b), buf_ptr, buf_bytes, ctypes.byref(o)),
+               "pa_sched_step_packed")
+        self._last_n = b.num_seqs
+        return b, o
 
     def complete(self, sampled) -> list:
         t = _tok(sampled)

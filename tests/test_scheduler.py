@@ -155,3 +155,64 @@ def test_requests_that_cannot_fit_are_refused(cpp_cls):
         ReferenceScheduler(4, 16).add_request(0, list(range(60)), 5)
     with pytest.raises(PAError):
         cpp_cls(4, 16).add_request(0, list(range(60)), 5)
+
+
+def test_packed_step_writes_the_same_batch_as_the_array_step(cpp_cls):
+    """pa_sched_step_packed: two schedulers fed the same requests and the same sampled tokens,
+    one stepped through separate arrays and one through one packed buffer, give equal
+    batches step by step (every array compared at the offsets the call reports, each on a
+    16-byte boundary, the device span first)."""
+    import ctypes
+    rng = np.random.default_rng(7)
+    a, b = cpp_cls(64, 16, 512, 128, 3), cpp_cls(64, 16, 512, 128, 3)
+    system = rng.integers(0, 500, size=48).tolist()
+    for rid in range(12):
+        p = (system if rid % 3 == 0 else []) + rng.integers(0, 500, size=int(rng.integers(5, 200))).tolist()
+        n = int(rng.integers(2, 20))
+        a.add_request(rid, p, n)
+        b.add_request(rid, p, n)
+    steps = 0
+    while True:
+        x = a.step()
+        buf = np.zeros(b.packed_bytes() // 8 + 2, dtype=np.int64)  # 16-byte aligned storage
+        ptr = buf.ctypes.data
+        assert ptr % 16 == 0
+        bt, o = b.step_packed(ptr, buf.nbytes)
+        assert x["kind"] == {0: "idle", 1: "prefill", 2: "decode"}[bt.kind]
+        if bt.kind == 0:
+            break
+        raw = buf.view(np.uint8)
+        S, T, W = bt.num_seqs, bt.num_tokens, bt.table_width
+        assert (S, T, bt.max_query_len, bt.max_context_len) == (x["num_seqs"], x["num_tokens"], x["max_query_len"],
+                                                                x["max_context_len"])
+        for name, off, dt, n in (("query_start_loc", o.query_start_loc, np.int32, S + 1),
+                                 ("context_lens", o.context_lens, np.int32, S),
+                                 ("slot_mapping", o.slot_mapping, np.int64, T),
+                                 ("token_ids", o.token_ids, np.int32, T), ("positions", o.positions, np.int32, T),
+                                 ("req_ids", o.req_ids, np.int64, S)):
+            assert off % 16 == 0
+            got = np.frombuffer(raw, dt, n, off)
+            assert np.array_equal(got, x[name]), name
+        tables = np.frombuffer(raw, np.int32, S * W, o.block_tables).reshape(S, W)
+        assert np.array_equal(tables, x["block_tables"])
+        pairs = np.frombuffer(raw, np.int64, 2 * bt.num_copy_pairs, o.copy_pairs).reshape(-1, 2)
+        assert np.array_equal(pairs, x["copy_pairs"])
+        assert max(o.query_start_loc, o.context_lens, o.block_tables, o.slot_mapping, o.copy_pairs, o.token_ids,
+                   o.positions) < o.dev_bytes <= o.req_ids < o.total_bytes <= buf.nbytes
+        sampled = rng.integers(0, 500, size=S).tolist()
+        a.complete(sampled)
+        b.complete(sampled)
+        steps += 1
+    assert steps > 10
+
+
+def test_packed_step_rejects_a_short_buffer(cpp_cls):
+    from paged_kv_attention_write_gb300 import PAError
+    s = cpp_cls(64, 16, 512, 128, 3)
+    s.add_request(0, list(range(100)), 4)
+    buf = np.zeros(4, dtype=np.int64)
+    with pytest.raises(PAError):
+        s.step_packed(buf.ctypes.data, buf.nbytes)
+    buf = np.zeros(s.packed_bytes() // 8 + 2, dtype=np.int64)
+    bt, _ = s.step_packed(buf.ctypes.data, buf.nbytes)   # nothing changed by the refused call
+    assert bt.kind == 1 and bt.num_tokens == 100
