@@ -68,14 +68,18 @@ class PagedAttentionEngine:
         self._dev_buf = None
         self._out = None
         self._ws = None
+        self._need = None
 
     def add_request(self, req_id: int, prompt, max_new_tokens: int) -> None:
         self.sched.add_request(req_id, prompt, max_new_tokens)
+        self._need = None  # the packed step may grow
 
     def _buffers(self):
         """The next pinned staging buffer (free once its previous copy has left it) and the
         device buffer, grown to the scheduler's packed size."""
-        need = self.sched.packed_bytes()
+        if self._need is None:
+            self._need = self.sched.packed_bytes()
+        need = self._need
         i = self._turn
         self._turn ^= 1
         if self._events[i] is not None:

@@ -170,6 +170,7 @@ class Scheduler:
         self._h = h
         self.block_size = block_size
         self._cap = None
+        self._fin = None
         self._last_n = 0
 
     def close(self) -> None:
@@ -232,12 +233,13 @@ class Scheduler:
 
     def complete(self, sampled) -> list:
         t = _tok(sampled)
-        b, _ = self._buffers()
+        ns = len(t)
+        if self._fin is None or len(self._fin) < max(1, ns):  # finished ids: at most one per sequence
+            self._fin = np.zeros(max(16, 2 * ns), dtype=np.int64)
         n = _i32()
-        _check(_lib.pa_sched_complete(self._h, t.ctypes.data if len(t) else None, len(t),
-                                      b["finished"].ctypes.data, len(b["finished"]), ctypes.byref(n)),
-               "pa_sched_complete")
-        return b["finished"][:n.value].tolist()
+        _check(_lib.pa_sched_complete(self._h, t.ctypes.data if ns else None, ns, self._fin.ctypes.data,
+                                      len(self._fin), ctypes.byref(n)), "pa_sched_complete")
+        return self._fin[:n.value].tolist()
 
     def stats(self) -> dict:
         out = np.zeros(7, dtype=np.int64)
