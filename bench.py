@@ -338,7 +338,7 @@ def prefill_arm(args, case, device, rank, world, dist_on):
     if rank != 0:
         return None
     tfs = flops / (ms_pf * 1e-3) / 1e12
-    return {
+    line = {
         "metric": "paged-attn chunked-prefill TFLOP/s (causal-exact FLOPs)",
         "value": round(world * flops / (ms_step * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
@@ -367,6 +367,9 @@ def prefill_arm(args, case, device, rank, world, dist_on):
         "clocks": clocks.summary(),
         "timed_region_s": round(wall, 3),
     }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = {**oracle_prefill_timing(), "kind": "oracle"}
+    return line
 
 
 def _barrier(dist_on):
