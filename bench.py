@@ -616,29 +616,38 @@ def _serve_replay(device, num_requests: int, seed: int):
         eng.add_request(rid, prompt, int(rng.integers(32, 257)))
     gpu = []
 
+    cb = [0.0]  # host seconds spent in the two callbacks (the stand-in model and sampler)
+
     def qkv(step):
         # the table row of each (token, position), from the step's device copy of both
-        # (int32 arithmetic: token < 32000 and position < 8192 keep the sum below 2^31)
+        # (int32 arithmetic: token < 32000 and position < 8192 keep the sum below 2^31;
+        # R is a power of two)
+        c0 = time.perf_counter()
         tok, pos = eng.device_tokens(step)
-        i = torch.remainder(tok * 7919 + pos * 104729, R)
+        i = torch.add(tok * 7919, pos, alpha=104729).bitwise_and_(R - 1)
         e = torch.cuda.Event(enable_timing=True)
         e.record()
         gpu.append([e, None])
-        return qt[i], kt[i], vt[i]
+        r = torch.index_select(qt, 0, i), torch.index_select(kt, 0, i), torch.index_select(vt, 0, i)
+        cb[0] += time.perf_counter() - c0
+        return r
 
     def sample(step, out):
+        c0 = time.perf_counter()
         e = torch.cuda.Event(enable_timing=True)
         e.record()
         gpu[-1][1] = e
         out[:, 0, 0].cpu()  # the step's result reaches the host (a sampler would need it)
-        return rng.integers(0, 32000, size=step["num_seqs"])
+        r = rng.integers(0, 32000, size=step["num_seqs"])
+        cb[0] += time.perf_counter() - c0
+        return r
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     steps = eng.run(qkv, sample)
     torch.cuda.synchronize()
     wall = time.perf_counter() - t0
     gpu_s = sum(a.elapsed_time(b) for a, b in gpu) / 1e3
-    return eng, steps, wall, gpu_s
+    return eng, steps, wall, gpu_s, cb[0]
 
 
 def serve_replay_measurement(device, num_requests: int = 256, seed: int = 11):
@@ -648,13 +657,18 @@ def serve_replay_measurement(device, num_requests: int = 256, seed: int = 11):
     depend on it).  One untimed warm-up replay first; reports generated tokens per second
     (seq-steps/s) end to end and the share of the wall time the step's kernels took."""
     _serve_replay(device, num_requests, seed)          # warm-up (lazy loading, allocator)
-    eng, steps, wall, gpu_s = _serve_replay(device, num_requests, seed)
+    eng, steps, wall, gpu_s, cb_s = _serve_replay(device, num_requests, seed)
     st, ms = eng.sched.stats(), eng.sched.manager_stats()
     return {"workload": SERVE_REPLAY, "steps": steps, "s": round(wall, 3),
             "seq_steps_per_s": round(st["generated_tokens"] / wall, 1),
             "prompt_tokens_per_s": round(st["prefill_tokens"] / wall, 1),
             "ms_per_step": round(wall / max(1, steps) * 1e3, 4),
             "kernel_share_of_wall": round(gpu_s / wall, 3),
+            "callbacks_ms_per_step": round(cb_s / max(1, steps) * 1e3, 4),
+            "engine_host_ms_per_step": round((wall - cb_s) / max(1, steps) * 1e3, 4),
+            "note": ("callbacks = the stand-in model and sampler (q/k/v gathers, the step's device read, "
+                     "which waits for the step's kernels); engine_host = the rest of the wall: "
+                     "scheduling, the packed copy and the attention call"),
             "scheduler": st, "kv_manager": ms, "warmup": "one untimed replay of the same workload"}
 
 

@@ -63,6 +63,7 @@ class PagedAttentionEngine:
                              num_heads, num_kv_heads, head_dim, self.dtype_code, self.scale)
         # two pinned staging buffers used in turn, each with the event of its last copy out
         self._pinned = [None, None]
+        self._pinned_np = [None, None]  # numpy views of the same memory
         self._events = [None, None]
         self._turn = 0
         self._dev_buf = None
@@ -86,6 +87,7 @@ class PagedAttentionEngine:
             self._events[i].synchronize()
         if self._pinned[i] is None or self._pinned[i].numel() < need:
             self._pinned[i] = torch.empty(2 * need, dtype=torch.uint8, pin_memory=True)
+            self._pinned_np[i] = self._pinned[i].numpy()
         if self._dev_buf is None or self._dev_buf.numel() < need:
             self._dev_buf = torch.empty(2 * need, dtype=torch.uint8, device=self.dev)
         return i
@@ -109,13 +111,14 @@ class PagedAttentionEngine:
             self.sched.complete([])  # close the idle step: requests added later can run
             return None
         S, T = b.num_seqs, b.num_tokens
-        stream = torch.cuda.current_stream().cuda_stream
+        cur = torch.cuda.current_stream(self.dev)
+        stream = cur.cuda_stream
         _check(_lib.pa_engine_upload(self._dev_buf.data_ptr(), host.data_ptr(), ctypes.byref(o), stream),
                "pa_engine_upload")
         if self._events[i] is None:
             self._events[i] = torch.cuda.Event()
-        self._events[i].record()
-        hb = host.numpy()
+        self._events[i].record(cur)
+        hb = self._pinned_np[i]
         step = {"kind": KIND_NAMES[b.kind], "num_seqs": S, "num_tokens": T,
                 "max_query_len": b.max_query_len, "max_context_len": b.max_context_len,
                 "req_ids": np.frombuffer(hb, np.int64, S, o.req_ids),
