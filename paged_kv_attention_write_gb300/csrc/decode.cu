@@ -1,6 +1,10 @@
 // decode.cu -- host side of paged decode: workspace layout, parameters, tensor maps,
 // and the plain (query not rotated) kernel instantiations.  The kernels and the
 // design are described in decode_kernels.cuh.
+#include <atomic>
+#include <chrono>
+#include <random>
+
 #include "decode_kernels.cuh"
 
 namespace pa {
@@ -12,7 +16,7 @@ size_t align_up(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct Layout {
     int HG, groups, HGq, K, C;
-    size_t seg, k0, m, l, o, total;
+    size_t seg, k0, m, l, o, tag, total;
 };
 
 Layout layout(int num_seqs, int num_heads, int num_kv_heads, int head_dim, int sms) {
@@ -28,8 +32,26 @@ Layout layout(int num_seqs, int num_heads, int num_kv_heads, int head_dim, int s
     L.m = L.k0 + align_up(sizeof(int32_t) * L.C);
     L.l = L.m + align_up(sizeof(float) * pieces);
     L.o = L.l + align_up(sizeof(float) * pieces);
-    L.total = L.o + align_up(sizeof(float) * pieces * head_dim);
+    L.tag = L.o + align_up(sizeof(float) * pieces * head_dim);
+    L.total = L.tag + align_up(sizeof(unsigned long long) * (1 + L.C + L.K));
     return L;
+}
+
+// A 64-bit value no earlier launch of this process used and that data left in a workspace
+// is vanishingly unlikely to hold: a counter mixed with a per-process seed through the
+// SplitMix64 finaliser (Steele, Lea and Flood, "Fast splittable pseudorandom number
+// generators", 2014).
+unsigned long long next_launch_tag() {
+    static std::atomic<unsigned long long> counter{0};
+    static const unsigned long long seed = [] {
+        std::random_device rd;
+        return ((unsigned long long)rd() << 32) ^ rd() ^
+               (unsigned long long)std::chrono::steady_clock::now().time_since_epoch().count();
+    }();
+    unsigned long long z = seed + 0x9E3779B97F4A7C15ull * (counter.fetch_add(1) + 1);
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+    return (z ^ (z >> 31)) | 1ull;
 }
 
 int grid_ctas() {
@@ -64,6 +86,8 @@ int launch_decode(const DecodeArgs &a) {
     prm.part_m = reinterpret_cast<float *>(ws + L.m);
     prm.part_l = reinterpret_cast<float *>(ws + L.l);
     prm.part_o = reinterpret_cast<float *>(ws + L.o);
+    prm.tags = reinterpret_cast<unsigned long long *>(ws + L.tag);
+    prm.launch_tag = next_launch_tag();
     prm.max_blocks_per_seq = a.max_blocks_per_seq;
     prm.num_seqs = a.num_seqs;
     prm.num_heads = a.num_heads;

@@ -55,6 +55,11 @@ struct DecodeParams {
     float *part_o;       // [(C + K) * HGq * D]
     float *part_m;       // [(C + K) * HGq]
     float *part_l;       // [(C + K) * HGq]
+    // launch tags (workspace): [0] the segment table is written, [1 + c + k] the partial of CTA c
+    // for segment k is written; each holds launch_tag once its data is visible
+    unsigned long long *tags;
+    unsigned long long launch_tag;
+    int scan_in_split;    // the split kernel's CTA 0 writes the segment table (else the plan kernel)
     int max_blocks_per_seq, num_seqs, num_heads, num_kv_heads, block_size, num_blocks;
     int max_context_len, head_dim;
     int heads_per_group;  // HG
@@ -221,6 +226,49 @@ __device__ __forceinline__ int owner_cta(int u, int N, int C) {
     return (int)((((int64_t)u + 1) * C + N - 1) / N) - 1;
 }
 
+// ------------------------------------------------------------------------------ launch tags
+
+__device__ __forceinline__ void store_release(unsigned long long *a, unsigned long long v) {
+    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(a), "l"(v) : "memory");
+}
+__device__ __forceinline__ unsigned long long load_acquire(const unsigned long long *a) {
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(a) : "memory");
+    return v;
+}
+// Loads that see other CTAs' writes made visible by a release the caller has acquired.
+__device__ __forceinline__ float load_relaxed(const float *a) {
+    float v;
+    asm volatile("ld.relaxed.gpu.global.f32 %0, [%1];" : "=f"(v) : "l"(a) : "memory");
+    return v;
+}
+__device__ __forceinline__ float2 load_relaxed2(const float *a) {
+    float2 v;
+    asm volatile("ld.relaxed.gpu.global.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "l"(a) : "memory");
+    return v;
+}
+__device__ __forceinline__ int load_relaxed_i(const int32_t *a) {
+    int v;
+    asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(a) : "memory");
+    return v;
+}
+
+// Wait until *a holds this launch's tag; false (and a status bit) after kWaitLimitNs.
+__device__ bool wait_tag(const unsigned long long *a, unsigned long long tag, int32_t *status) {
+    if (load_acquire(a) == tag) return true;
+    const unsigned long long t0 = global_ns();
+    unsigned ns = 32;
+    for (;;) {
+        __nanosleep(ns);
+        if (ns < 256) ns *= 2;
+        if (load_acquire(a) == tag) return true;
+        if (global_ns() - t0 > kWaitLimitNs) {
+            report(status, PA_DEVERR_TIMEOUT);
+            return false;
+        }
+    }
+}
+
 // ------------------------------------------------------------------------------ plan kernel
 
 __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const DecodeParams p) {
@@ -274,6 +322,10 @@ __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const DecodeP
     const int N = carry;
     if (tid == 0) p.seg_start[K] = N;
     __syncthreads();  // seg_start is visible to the whole block
+    if (tid == 0) {   // and, once this fence is passed, to the reduce kernel
+        __threadfence();
+        store_release(p.tags, p.launch_tag);
+    }
     // CTA c starts at unit c*N/C, inside the segment k with seg_start[k] <= c*N/C <
     // seg_start[k+1]: the CTAs starting in segment k are ceil(beg*C/N) .. ceil(end*C/N)-1.
     const int C = min(p.grid, N);
@@ -345,6 +397,11 @@ __device__ void publish_scan(const DecodeParams &p, const int *sseg, int K, int 
     const int ob = p.out_dtype == PA_F32 ? 4 : 2;
     const int words = HGq * p.head_dim * ob / 4;
     for (int k = threadIdx.x; k <= K; k += kDecodeThreads) p.seg_start[k] = sseg[k];
+    __syncthreads();
+    if (threadIdx.x == 0) {  // the reduce kernel may read the table
+        __threadfence();
+        store_release(p.tags, p.launch_tag);
+    }
     for (int k = threadIdx.x; k < K; k += kDecodeThreads) {
         if (sseg[k] != sseg[k + 1]) continue;
         const int s = k % S, hg = k / S;
@@ -674,9 +731,14 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
         __syncwarp();
     };
 
+    // The segments whose partial this CTA writes (its first and its last at most); their launch
+    // tags are published once the CTA has streamed its whole range.
+    int part0 = -1, part1 = -1;
+
     // Write this CTA's piece of segment k: merge lane groups and token slices,
     // then the output (whole segment here) or a partial for the reduce kernel.
     auto flush = [&](int k, bool whole) {
+        if (!whole) (part0 < 0 ? part0 : part1) = k;
 #pragma unroll
         for (int o = LPT; o < 32; o <<= 1)
 #pragma unroll
@@ -821,67 +883,103 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
         if (lane == 0) mbar_arrive(empty0 + 8 * stage);
         if (u == seg_end - 1 || u == u1 - 1) flush(k, seg_beg >= u0 && seg_end <= u1);
     }
+    // Every consumer warp's partial stores are done; one thread makes them visible at GPU
+    // scope and publishes this launch's tag for each of the CTA's partials.
+    named_barrier(1, NW * 32);
+    if (warp == 0 && lane == 0 && part0 >= 0) {
+        __threadfence();
+        store_release(p.tags + 1 + c + part0, p.launch_tag);
+        if (part1 >= 0) store_release(p.tags + 1 + c + part1, p.launch_tag);
+    }
 }
 
 // ------------------------------------------------------------------------------ reduce kernel
 
 constexpr int kMaxPieces = 1024;  // CTAs of the split kernel (one per SM)
-constexpr int kReduceBatch = 32;  // pieces whose loads are in flight together
+constexpr int kReduceBatch = 16;  // pieces whose loads are in flight together
 
 // For every segment split over several CTAs: out = sum_c 2^(m_c - M) acc_c /
 // sum_c 2^(m_c - M) l_c.  grid = (segment, group of blockDim.y query heads of the
 // group); one thread per pair of outputs of one head.  The launcher packs up to
-// kReduceHeads heads per CTA while that still leaves about a wave of CTAs, so that few
-// small CTAs have to be scheduled after the split kernel.  The loads of a batch of pieces are all issued before
-// any is used (two memory round trips for the usual segment of < 32 pieces), and the
-// batch is merged online (running max).
-constexpr int kReduceHeads = 8;
+// kReduceHeads heads per CTA while that still leaves about a wave of CTAs; the CTAs are
+// small so that they fit beside the split kernel's and can wait there.  A CTA waits for
+// the launch tags of its segment's pieces, not for the split grid to end, then issues the
+// loads of a batch of pieces before using any (one round trip for a segment of up to
+// kReduceBatch pieces) and merges the batch online (running max).
+constexpr int kReduceHeads = 2;
 template <int D>
 __global__ void __launch_bounds__(D / 2 * kReduceHeads) decode_reduce_kernel(const DecodeParams p, int HGq) {
-    pdl_wait_previous();
+    // The partials are awaited piece by piece (their launch tags) rather than through the end
+    // of the split grid, so that a segment merges as soon as its own CTAs have written it;
+    // the wait for the split grid comes last, so that this grid still ends after it.
+    __shared__ int ready;
+    const int tid = threadIdx.y * blockDim.x + threadIdx.x;
     const int k = blockIdx.x, hl = blockIdx.y * blockDim.y + threadIdx.y, d = threadIdx.x * 2;
-    if (hl >= HGq) return;
     const int S = p.num_seqs, K = p.num_groups * S;
-    const int N = p.seg_start[K];
-    const int beg = p.seg_start[k], end = p.seg_start[k + 1];
-    if (beg == end) return;  // zero row written by the plan kernel
-    const int C = min(p.grid, N);
-    const int c_lo = owner_cta(beg, N, C), c_hi = owner_cta(end - 1, N, C);
-    if (c_lo == c_hi) return;  // written by the split kernel
-    const int n = c_hi - c_lo + 1;
-    const int64_t base = (int64_t)(c_lo + k) * HGq + hl;  // piece j is base + j * HGq
-    float M = -INFINITY, L = 0.f, o0 = 0.f, o1 = 0.f;
-    for (int j0 = 0; j0 < n; j0 += kReduceBatch) {
-        float mj[kReduceBatch], lj[kReduceBatch];
-        float2 oj[kReduceBatch];
-#pragma unroll
-        for (int i = 0; i < kReduceBatch; ++i) {
-            const int64_t pi = base + (int64_t)(j0 + i) * HGq;
-            const bool ok = j0 + i < n;
-            mj[i] = ok ? __ldg(p.part_m + pi) : -INFINITY;
-            lj[i] = ok ? __ldg(p.part_l + pi) : 0.f;
-            oj[i] = ok ? *reinterpret_cast<const float2 *>(p.part_o + pi * D + d) : make_float2(0.f, 0.f);
-        }
-        float bm = M;
-#pragma unroll
-        for (int i = 0; i < kReduceBatch; ++i) bm = fmaxf(bm, mj[i]);
-        const float a = fast_exp2(M - bm);  // 0 on the first batch
-        L *= a;
-        o0 *= a;
-        o1 *= a;
-#pragma unroll
-        for (int i = 0; i < kReduceBatch; ++i) {
-            const float f = fast_exp2(mj[i] - bm);  // 0 for padding entries
-            L = fmaf(lj[i], f, L);
-            o0 = fmaf(oj[i].x, f, o0);
-            o1 = fmaf(oj[i].y, f, o1);
-        }
-        M = bm;
+    if (p.scan_in_split) {
+        if (tid == 0) ready = wait_tag(p.tags, p.launch_tag, p.status);
+    } else {
+        pdl_wait_previous();  // the plan kernel wrote the table before the split kernel began
+        if (tid == 0) ready = 1;
     }
-    const float inv = 1.f / L;
-    const int s = k % S, hg = k / S;
-    store_pair_any(p.out, p.out_dtype, ((int64_t)s * p.num_heads + hg * HGq + hl) * D + d, o0 * inv,
-                   o1 * inv);
+    __syncthreads();
+    int c_lo = 0, n = 0;
+    if (ready) {
+        const int N = load_relaxed_i(p.seg_start + K);
+        const int beg = load_relaxed_i(p.seg_start + k), end = load_relaxed_i(p.seg_start + k + 1);
+        if (beg != end) {  // else a zero row, written by the split or plan kernel
+            const int C = min(p.grid, N);
+            c_lo = owner_cta(beg, N, C);
+            const int c_hi = owner_cta(end - 1, N, C);
+            n = c_hi > c_lo ? c_hi - c_lo + 1 : 0;  // one piece: written by the split kernel
+        }
+    }
+    if (n > 0) {  // the same in every thread of the CTA
+        __syncthreads();  // every thread has read `ready`
+        if (tid < 32) {   // lane j waits for the pieces j, j + 32, ...
+            bool all = true;
+            for (int j = tid; j < n; j += 32) all = wait_tag(p.tags + 1 + c_lo + k + j, p.launch_tag, p.status) && all;
+            all = __all_sync(kFullMask, all);
+            if (tid == 0) ready = all;
+        }
+        __syncthreads();
+        if (ready && hl < HGq) {
+            const int64_t base = (int64_t)(c_lo + k) * HGq + hl;  // piece j is base + j * HGq
+            float M = -INFINITY, L = 0.f, o0 = 0.f, o1 = 0.f;
+            for (int j0 = 0; j0 < n; j0 += kReduceBatch) {
+                float mj[kReduceBatch], lj[kReduceBatch];
+                float2 oj[kReduceBatch];
+#pragma unroll
+                for (int i = 0; i < kReduceBatch; ++i) {
+                    const int64_t pi = base + (int64_t)(j0 + i) * HGq;
+                    const bool ok = j0 + i < n;
+                    mj[i] = ok ? load_relaxed(p.part_m + pi) : -INFINITY;
+                    lj[i] = ok ? load_relaxed(p.part_l + pi) : 0.f;
+                    oj[i] = ok ? load_relaxed2(p.part_o + pi * D + d) : make_float2(0.f, 0.f);
+                }
+                float bm = M;
+#pragma unroll
+                for (int i = 0; i < kReduceBatch; ++i) bm = fmaxf(bm, mj[i]);
+                const float a = fast_exp2(M - bm);  // 0 on the first batch
+                L *= a;
+                o0 *= a;
+                o1 *= a;
+#pragma unroll
+                for (int i = 0; i < kReduceBatch; ++i) {
+                    const float f = fast_exp2(mj[i] - bm);  // 0 for padding entries
+                    L = fmaf(lj[i], f, L);
+                    o0 = fmaf(oj[i].x, f, o0);
+                    o1 = fmaf(oj[i].y, f, o1);
+                }
+                M = bm;
+            }
+            const float inv = 1.f / L;
+            const int s = k % S, hg = k / S;
+            store_pair_any(p.out, p.out_dtype, ((int64_t)s * p.num_heads + hg * HGq + hl) * D + d, o0 * inv,
+                           o1 * inv);
+        }
+    }
+    pdl_wait_previous();  // this grid ends after the split kernel (whose whole segments it does not await)
 }
 
 template <class T, int D, int G, bool ROPE>
@@ -891,6 +989,7 @@ int launch_typed(DecodeParams prm, const CUtensorMap &km, const CUtensorMap &vm,
     prm.unit_tokens = Sh::NT * (kConsumerWarps / prm.heads_per_group);
     prm.box_rows = prm.block_size < prm.unit_tokens ? prm.block_size : prm.unit_tokens;
     const bool fused = prm.num_groups * prm.num_seqs < kSegSmem;  // scan inside the split kernel
+    prm.scan_in_split = fused ? 1 : 0;
     // reduce: heads per CTA, as many as keep about 128 CTAs (one wave)
     const int K = prm.num_groups * prm.num_seqs, HGq = prm.heads_per_group * G;
     int rh = kReduceHeads;
