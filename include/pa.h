@@ -132,8 +132,10 @@ size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads, i
  *                  used to size the split of the context)
  *   scale          softmax scale applied to q.k (normally 1/sqrt(head_dim))
  *   workspace      device scratch of >= pa_decode_workspace_size(...) bytes,
- *                  16-byte aligned, owned by the caller; its contents are
- *                  clobbered, and two calls in flight must not share it
+ *                  16-byte aligned, owned by the caller; it needs no
+ *                  initialisation (each call marks what it writes with its own
+ *                  64-bit tag), its contents are clobbered, and two calls in
+ *                  flight must not share it
  *
  *   out[s][h] = sum_j softmax_j(scale * q[s][h] . k_j) v_j over j < context_lens[s];
  *   a sequence with context length 0 gets an all-zero row.

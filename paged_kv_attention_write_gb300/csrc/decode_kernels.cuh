@@ -26,6 +26,12 @@
 // for the reduce); beyond that a one-CTA plan kernel computes it first.  The
 // scan's owner also clamps the context lengths (reporting bad ones) and zeroes
 // the output of sequences with nothing to attend.
+// The reduce does not wait for the end of the split grid before merging: each launch
+// carries a 64-bit tag, the scan's owner and every CTA with partials store it (release)
+// once their data is visible, and a reduce CTA -- small enough to be resident beside a
+// split CTA -- waits (acquire, bounded in time) for the tags of its segment's pieces.
+// It waits for the split grid only before it exits, so that the reduce grid still ends
+// after every output the split kernel writes directly.
 //
 // Split kernel, per CTA: one producer warp issues 3-D TMA loads of whole
 // [tokens][HG heads][D] boxes of K and V (one box per block piece, taken
