@@ -146,6 +146,48 @@ def test_decode_result_independent_of_split(oracle_mod):
         assert (r - rows[0]).abs().max().item() <= 1e-5
 
 
+def test_decode_workspace_needs_no_initialisation_and_old_launches_never_count(oracle_mod):
+    """One workspace, first filled with random bytes, shared by a 32-sequence call, a call on
+    8 of its sequences and, after the workspace is put back to what the first call left in it
+    (its partials and its launch tags), the first shape again with another query: the reduce
+    must wait for this launch's pieces, never take the earlier launch's.  Every call against
+    the oracle."""
+    import paged_kv_attention_write_gb300 as pa
+    rng = np.random.default_rng(23)
+    lens = [9000] + [int(x) for x in rng.integers(2000, 5000, size=7)] + \
+           [int(x) for x in rng.integers(100, 1500, size=24)]
+    case = workloads.make_decode_case("reuse", lens, 32, 32, 8, 128, torch.bfloat16, 23)
+    kc, vc = case.key_cache.cuda(), case.value_cache.cuda()
+    pa.pa_reshape_and_cache(case.new_key.cuda(), case.new_value.cuda(), kc, vc, case.slot_mapping.cuda())
+    _, okc, ovc = oracle_step(case, oracle_mod)
+    S, Hq, D = case.query.shape
+    n = pa.pa_decode_workspace_size(S, case.num_heads, case.num_kv_heads, D, int(case.context_lens.max()))
+    ws = torch.from_numpy(rng.integers(0, 256, size=n, dtype=np.uint8)).cuda()
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+
+    def run(q, seqs):
+        idx = torch.tensor(seqs, dtype=torch.int64)
+        mcl = int(case.context_lens[idx].max())
+        out = torch.full((len(seqs), Hq, D), float("nan"), dtype=torch.float32, device="cuda")
+        pa.pa_decode(out, q[idx].contiguous().cuda(), kc, vc, case.block_tables[idx].contiguous().cuda(),
+                     case.context_lens[idx].contiguous().cuda(), mcl, case.scale, workspace=ws, status=status)
+        torch.cuda.synchronize()
+        assert status.item() == 0
+        ref = oracle_mod.paged_attention(q[idx], torch.arange(len(seqs) + 1, dtype=torch.int32), okc, ovc,
+                                         case.block_tables[idx], case.context_lens[idx], case.scale)
+        assert_attention_close(out.cpu(), ref)
+        return out.cpu()
+
+    every = list(range(S))
+    q2 = torch.from_numpy(rng.standard_normal(tuple(case.query.shape)).astype(np.float32)).to(case.query.dtype)
+    first = run(case.query, every)
+    left = ws.clone()
+    run(case.query, list(range(0, S, 4)))
+    ws.copy_(left)
+    again = run(q2, every)
+    assert (again - first).abs().max().item() > 0.1  # the new query's rows, not the old ones
+
+
 @pytest.mark.parametrize("out_dtype", [torch.float16, torch.bfloat16])
 def test_decode_low_precision_output_is_rounded_fp32(oracle_mod, out_dtype):
     case = workloads.make_decode_case("o", [100, 1000, 3000], 32, 32, 8, 128, torch.bfloat16, 4)
