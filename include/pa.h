@@ -149,6 +149,36 @@ int pa_decode(void *out, pa_dtype out_dtype, const void *query, const void *key_
               pa_stream_t stream);
 
 /*
+ * pa_decode_write -- pa_reshape_and_cache of one new token per sequence followed by
+ * pa_decode, in one launch (the decode step of a serving loop: the TensorSharp "Mistral 3"
+ * page, section 11, writes the step's K/V through slotMapping, then attends).
+ *
+ *   key, value     [num_seqs][num_kv_heads][head_dim], kv_dtype (device): token s is the
+ *                  newest token of sequence s
+ *   slot_mapping   int64 [num_seqs]: its cache slot (blockId * block_size + offset); a
+ *                  negative slot writes nothing, a slot past the pool is reported
+ *                  (PA_DEVERR_SLOT) and not written
+ *   key_cache,
+ *   value_cache    written at those slots, then read as by pa_decode
+ *   (every other argument as for pa_decode)
+ *
+ * Precondition (the decode step of any paged KV manager): slot_mapping[s] is the slot that
+ * block_tables[s] gives position context_lens[s] - 1, and no other sequence of the call
+ * reads that slot (a block being appended to is never shared).  Then out and both pools
+ * equal those of pa_reshape_and_cache(key, value, ..., slot_mapping, num_seqs, ...) and
+ * pa_decode(...) on the same stream, bit for bit.  Otherwise the pools are written as
+ * stated and out is unspecified.  The launch that streams a sequence's last keys stores
+ * the token and uses it from the same copy, so no kernel boundary separates the two.
+ */
+int pa_decode_write(void *out, pa_dtype out_dtype, const void *query, const void *key,
+                    const void *value, const int64_t *slot_mapping, void *key_cache,
+                    void *value_cache, const int32_t *block_tables, int max_blocks_per_seq,
+                    const int32_t *context_lens, int max_context_len, int num_seqs, int num_heads,
+                    int num_kv_heads, int head_dim, int block_size, int num_blocks, float scale,
+                    pa_dtype kv_dtype, void *workspace, size_t workspace_bytes, int32_t *status,
+                    pa_stream_t stream);
+
+/*
  * pa_decode_noalloc -- pa_decode for callers that cannot allocate device
  * memory: plugin hosts and serving runtimes that own all device memory and hand
  * kernels only their tensors, hot paths where a cudaMalloc could synchronise

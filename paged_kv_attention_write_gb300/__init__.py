@@ -28,7 +28,7 @@ import torch
 __all__ = [
     "PAError", "pa_reshape_and_cache", "pa_decode_workspace_size", "pa_decode", "pa_decode_noalloc",
     "pa_prefill_chunk", "pa_copy_blocks", "pa_status_string", "pa_version", "library_path",
-    "Rope", "pa_rope_yarn_freqs", "pa_reshape_and_cache_rope", "pa_decode_rope",
+    "Rope", "pa_rope_yarn_freqs", "pa_reshape_and_cache_rope", "pa_decode_rope", "pa_decode_write",
     "PA_F32", "PA_F16", "PA_BF16",
 ]
 
@@ -54,6 +54,8 @@ _lib.pa_decode_noalloc.argtypes = [_vp, _i32, _vp, _vp, _vp, _vp, _i32, _vp, _i3
 _lib.pa_prefill_chunk.argtypes = [_vp, _i32, _vp, _vp, _i32, _i32, _vp, _vp, _vp, _i32, _vp, _i32,
                                   _i32, _i32, _i32, _i32, _i32, _i32, _f32, _i32, _vp, _vp]
 _lib.pa_copy_blocks.argtypes = [_vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _vp, _vp]
+_lib.pa_decode_write.argtypes = [_vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32,
+                                 _i32, _i32, _i32, _i32, _f32, _i32, _vp, _sz, _vp, _vp]
 _lib.pa_status_string.argtypes = [_i32]
 _lib.pa_status_string.restype = ctypes.c_char_p
 _lib.pa_version.argtypes = []
@@ -70,7 +72,7 @@ _lib.pa_decode_rope.argtypes = [_vp, _i32, _vp, _vp, _vp, _vp, _i32, _vp, _i32, 
                                 _i32, _i32, _f32, _i32, ctypes.POINTER(_PaRope), _vp, _sz, _vp, _vp]
 for _name in ("pa_reshape_and_cache", "pa_decode", "pa_decode_noalloc", "pa_prefill_chunk",
               "pa_copy_blocks", "pa_version", "pa_rope_yarn_freqs", "pa_reshape_and_cache_rope",
-              "pa_decode_rope"):
+              "pa_decode_rope", "pa_decode_write"):
     getattr(_lib, _name).restype = _i32
 
 
@@ -143,6 +145,21 @@ def pa_decode(out, query, key_cache, value_cache, block_tables, context_lens, ma
                           int(max_context_len), S, Hq, Hkv, D, bs, NB, float(scale),
                           _dt(key_cache), _ptr(workspace), ws_bytes, _ptr(status),
                           _stream(stream)), "pa_decode")
+
+
+def pa_decode_write(out, query, key, value, slot_mapping, key_cache, value_cache, block_tables,
+                    context_lens, max_context_len: int, scale: float, *, workspace=None, status=None,
+                    stream=None) -> None:
+    """pa_reshape_and_cache of each sequence's new token (key / value ``[S][Hkv][D]`` to
+    ``slot_mapping[s]``) and pa_decode, in one launch."""
+    S, Hq, D = query.shape
+    NB, bs, Hkv, _ = key_cache.shape
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(_lib.pa_decode_write(_ptr(out), _dt(out), _ptr(query), _ptr(key), _ptr(value), _ptr(slot_mapping),
+                                _ptr(key_cache), _ptr(value_cache), _ptr(block_tables), block_tables.shape[1],
+                                _ptr(context_lens), int(max_context_len), S, Hq, Hkv, D, bs, NB, float(scale),
+                                _dt(key_cache), _ptr(workspace), ws_bytes, _ptr(status), _stream(stream)),
+           "pa_decode_write")
 
 
 def pa_decode_noalloc(out, query, key_cache, value_cache, block_tables, context_lens,

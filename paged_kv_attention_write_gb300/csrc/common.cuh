@@ -210,6 +210,9 @@ struct DecodeArgs {
     int rope_dim = 0;
     float q_scale_beta = 0.f;
     int q_scale_orig_ctx = 0;
+    // the new token of every sequence, written to its slot first (null key: no write)
+    const void *new_key = nullptr, *new_value = nullptr;
+    const int64_t *slot_mapping = nullptr;
 };
 
 struct PrefillArgs {

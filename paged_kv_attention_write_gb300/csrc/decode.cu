@@ -105,6 +105,12 @@ int launch_decode(const DecodeArgs &a) {
     prm.rope_dim = a.rope_dim;
     prm.q_scale_beta = a.q_scale_beta;
     prm.q_scale_orig_ctx = a.q_scale_orig_ctx;
+    prm.new_key = a.new_key;
+    prm.new_value = a.new_value;
+    prm.slot_mapping = a.slot_mapping;
+    prm.key_cache_w = const_cast<void *>(a.key_cache);
+    prm.value_cache_w = const_cast<void *>(a.value_cache);
+    prm.num_slots = (int64_t)a.num_blocks * a.block_size;
 
     // box rows are set per instantiation (they depend on the stage shape); encode the
     // tensor maps with the largest box the shape can use and re-encode if smaller.
@@ -121,8 +127,9 @@ int launch_decode(const DecodeArgs &a) {
         make_kv_tensor_map(&vm, a.value_cache, a.kv_dtype, a.head_dim, a.num_kv_heads, pool_rows,
                            L.HG, rows) != PA_OK)
         return PA_ERR_CUDA;
-    return a.rope_freqs ? dispatch_decode_rope(prm, a.kv_dtype, a.head_dim, G, km, vm, a.stream)
-                        : dispatch_kv<false>(prm, a.kv_dtype, a.head_dim, G, km, vm, a.stream);
+    if (a.rope_freqs) return dispatch_decode_rope(prm, a.kv_dtype, a.head_dim, G, km, vm, a.stream);
+    if (a.new_key) return dispatch_decode_write(prm, a.kv_dtype, a.head_dim, G, km, vm, a.stream);
+    return dispatch_kv<false>(prm, a.kv_dtype, a.head_dim, G, km, vm, a.stream);
 }
 
 }  // namespace pa

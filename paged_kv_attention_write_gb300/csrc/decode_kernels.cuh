@@ -80,12 +80,21 @@ struct DecodeParams {
     int rope_dim;
     float q_scale_beta;
     int q_scale_orig_ctx;
+    // cache write fused in front of the attention (pa_decode_write): the new token of every
+    // sequence, [S][Hkv][D] in the cache's type, stored at slot_mapping[s]
+    const void *new_key, *new_value;
+    const int64_t *slot_mapping;
+    void *key_cache_w, *value_cache_w;
+    int64_t num_slots;
 };
 
 // The launchers of the query-rotating instantiations (decode_rope.cu); the plain ones
 // are instantiated in decode.cu.  Both take the parameters launch_decode prepared.
 int dispatch_decode_rope(const DecodeParams &prm, pa_dtype kv_dtype, int D, int G, const CUtensorMap &km,
                          const CUtensorMap &vm, cudaStream_t st);
+// ... and of the instantiations that write each sequence's new token first (decode_write.cu).
+int dispatch_decode_write(const DecodeParams &prm, pa_dtype kv_dtype, int D, int G, const CUtensorMap &km,
+                          const CUtensorMap &vm, cudaStream_t st);
 
 namespace {
 
@@ -224,6 +233,10 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
                  : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                  : "r"(addr));
     return v;
+}
+__device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
 }
 
 // CTA that owns unit u when N units are split over C CTAs (CTA c owns
@@ -419,7 +432,7 @@ __device__ void publish_scan(const DecodeParams &p, const int *sseg, int K, int 
 
 // ------------------------------------------------------------------------------ split kernel
 
-template <class T, int D, int G, bool ROPE>
+template <class T, int D, int G, bool ROPE, bool WRITE>
 __global__ void __launch_bounds__(kDecodeThreads, 1)
 decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                     const DecodeParams p) {
@@ -836,6 +849,40 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
         reset();
     };
 
+    // Fused cache write: the CTA that streams a segment's last unit stores the sequence's new
+    // token (position context_len - 1) into its cache slot and patches the token's rows into
+    // that unit's shared-memory stage, so that its own scores never depend on the store having
+    // landed; only the warp whose token slice holds the token does it, one 16-byte slice per
+    // lane.  A negative slot writes nothing (the stage keeps what the cache holds), like
+    // pa_reshape_and_cache.
+    [[maybe_unused]] uint4 new_k{}, new_v{};
+    [[maybe_unused]] int patch_tn = -1;  // stage row of the new token in the segment's last unit
+    auto new_token = [&](int s, int hg, int ctx, int seg_beg, int seg_end) {
+        if constexpr (WRITE) {
+            patch_tn = -1;
+            if (seg_end > u1 || ctx <= 0 || p.context_lens[s] != ctx) return;  // not ours, or clamped
+            const int tn = (ctx - 1) - (seg_end - 1 - seg_beg) * TU;
+            if (tn / NT != sb) return;
+            const int64_t slot = p.slot_mapping[s];
+            if (slot < 0) return;
+            if (slot >= p.num_slots) {
+                if (lane == 0) report(p.status, PA_DEVERR_SLOT);
+                return;
+            }
+            patch_tn = tn;
+            if (grp == 0) {
+                const int64_t head = (int64_t)hg * HG + h;
+                const int64_t src = ((int64_t)s * p.num_kv_heads + head) * D + r * EPV;
+                const int64_t dst = (slot * p.num_kv_heads + head) * D + r * EPV;
+                using ST = typename T::storage;
+                new_k = ldg_stream(reinterpret_cast<const uint4 *>(static_cast<const ST *>(p.new_key) + src));
+                new_v = ldg_stream(reinterpret_cast<const uint4 *>(static_cast<const ST *>(p.new_value) + src));
+                *reinterpret_cast<uint4 *>(static_cast<ST *>(p.key_cache_w) + dst) = new_k;
+                *reinterpret_cast<uint4 *>(static_cast<ST *>(p.value_cache_w) + dst) = new_v;
+            }
+        }
+    };
+
     reset();
     int k = k0, seg_beg = segs[k], seg_end = segs[k + 1];
     int s = k % S, hg = k / S, ctx = context_of(s);
@@ -844,6 +891,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
         q_global(s, hg, raw);
         load_q(raw, ctx);
     }
+    new_token(s, hg, ctx, seg_beg, seg_end);
     bool pf_pending = false;
     int pf_ctx = 0;
     for (int u = u0, i = 0; u < u1; ++u, ++i) {
@@ -865,6 +913,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
                 q_global(s, hg, raw);
             }
             load_q(raw, ctx);
+            new_token(s, hg, ctx, seg_beg, seg_end);
         }
         if (q_prefetch && u + 1 == seg_end && u + 1 < u1) {  // the next unit starts a segment
             int kn = k + 1;
@@ -877,13 +926,29 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
         const uint32_t parity = (i / NSTAGE) & 1;
         const bool ok = !*abort_v && mbar_wait(full0 + 8 * stage, parity, p.status);
         if (!ok) *abort_v = 1;
+        [[maybe_unused]] bool patched = false;
         if (ok) {
             const uint32_t kbase = stage_base + stage * 2 * KVB, vbase = kbase + KVB;
+            if constexpr (WRITE) {
+                if (patch_tn >= 0 && u == seg_end - 1) {  // the new token's rows into the stage
+                    if (grp == 0) {
+                        const uint32_t off = (uint32_t)((patch_tn * HG + h) * ROWB + r * 16);
+                        sts128(kbase + off, new_k);
+                        sts128(vbase + off, new_v);
+                    }
+                    __syncwarp();
+                    patched = true;
+                }
+            }
             const int tok0 = (u - seg_beg) * TU + sb * NT;
             if (tok0 + NT <= ctx)
                 consume(kbase, vbase, tok0, ctx, std::false_type{});
             else if (tok0 < ctx)
                 consume(kbase, vbase, tok0, ctx, std::true_type{});
+        }
+        if constexpr (WRITE) {
+            // the stage is written by TMA (the async proxy) again after this warp releases it
+            if (patched) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(empty0 + 8 * stage);
@@ -988,7 +1053,7 @@ __global__ void __launch_bounds__(D / 2 * kReduceHeads) decode_reduce_kernel(con
     pdl_wait_previous();  // this grid ends after the split kernel (whose whole segments it does not await)
 }
 
-template <class T, int D, int G, bool ROPE>
+template <class T, int D, int G, bool ROPE, bool WRITE>
 int launch_typed(DecodeParams prm, const CUtensorMap &km, const CUtensorMap &vm, cudaStream_t st) {
     using Sh = DecodeShape<T, D, G>;
     static std::atomic<int> smem_ready[kMaxDevices];  // per device: shared-memory limit raised
@@ -1002,7 +1067,7 @@ int launch_typed(DecodeParams prm, const CUtensorMap &km, const CUtensorMap &vm,
     while (rh > 1 && (int64_t)K * ((HGq + rh - 1) / rh) < 128) rh >>= 1;
     if ((!fused &&
          launch_pdl(decode_plan_kernel, dim3(1), dim3(kPlanThreads), 0, st, prm) != cudaSuccess) ||
-        launch_pdl_smem(decode_split_kernel<T, D, G, ROPE>, smem_ready, dim3(prm.grid), dim3(kDecodeThreads),
+        launch_pdl_smem(decode_split_kernel<T, D, G, ROPE, WRITE>, smem_ready, dim3(prm.grid), dim3(kDecodeThreads),
                         Sh::SMEM, st, km, vm, prm) != cudaSuccess ||
         launch_pdl(decode_reduce_kernel<D>, dim3(K, (HGq + rh - 1) / rh), dim3(D / 2, rh), 0, st, prm, HGq) !=
             cudaSuccess)
@@ -1010,36 +1075,36 @@ int launch_typed(DecodeParams prm, const CUtensorMap &km, const CUtensorMap &vm,
     return PA_OK;
 }
 
-template <class T, int D, bool ROPE>
+template <class T, int D, bool ROPE, bool WRITE>
 int dispatch_g(const DecodeParams &prm, int G, const CUtensorMap &km, const CUtensorMap &vm,
                cudaStream_t st) {
     switch (G) {
-        case 1: return launch_typed<T, D, 1, ROPE>(prm, km, vm, st);
-        case 2: return launch_typed<T, D, 2, ROPE>(prm, km, vm, st);
-        case 4: return launch_typed<T, D, 4, ROPE>(prm, km, vm, st);
-        case 8: return launch_typed<T, D, 8, ROPE>(prm, km, vm, st);
+        case 1: return launch_typed<T, D, 1, ROPE, WRITE>(prm, km, vm, st);
+        case 2: return launch_typed<T, D, 2, ROPE, WRITE>(prm, km, vm, st);
+        case 4: return launch_typed<T, D, 4, ROPE, WRITE>(prm, km, vm, st);
+        case 8: return launch_typed<T, D, 8, ROPE, WRITE>(prm, km, vm, st);
         default: return PA_ERR_UNSUPPORTED;
     }
 }
 
-template <class T, bool ROPE>
+template <class T, bool ROPE, bool WRITE>
 int dispatch_d(const DecodeParams &prm, int D, int G, const CUtensorMap &km, const CUtensorMap &vm,
                cudaStream_t st) {
     switch (D) {
-        case 64: return dispatch_g<T, 64, ROPE>(prm, G, km, vm, st);
-        case 128: return dispatch_g<T, 128, ROPE>(prm, G, km, vm, st);
+        case 64: return dispatch_g<T, 64, ROPE, WRITE>(prm, G, km, vm, st);
+        case 128: return dispatch_g<T, 128, ROPE, WRITE>(prm, G, km, vm, st);
         default: return PA_ERR_UNSUPPORTED;
     }
 }
 
 // Typed dispatch of one decode call on the cache format, head dim and group size.
-template <bool ROPE>
+template <bool ROPE, bool WRITE = false>
 int dispatch_kv(const DecodeParams &prm, pa_dtype kv_dtype, int D, int G, const CUtensorMap &km,
                 const CUtensorMap &vm, cudaStream_t st) {
     switch (kv_dtype) {
-        case PA_F32: return dispatch_d<F32, ROPE>(prm, D, G, km, vm, st);
-        case PA_F16: return dispatch_d<F16, ROPE>(prm, D, G, km, vm, st);
-        case PA_BF16: return dispatch_d<BF16, ROPE>(prm, D, G, km, vm, st);
+        case PA_F32: return dispatch_d<F32, ROPE, WRITE>(prm, D, G, km, vm, st);
+        case PA_F16: return dispatch_d<F16, ROPE, WRITE>(prm, D, G, km, vm, st);
+        case PA_BF16: return dispatch_d<BF16, ROPE, WRITE>(prm, D, G, km, vm, st);
     }
     return PA_ERR_UNSUPPORTED;
 }

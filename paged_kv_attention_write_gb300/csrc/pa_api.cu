@@ -138,6 +138,32 @@ int pa_decode(void *out, pa_dtype out_dtype, const void *query, const void *key_
     return pa::launch_decode(a);
 }
 
+int pa_decode_write(void *out, pa_dtype out_dtype, const void *query, const void *key, const void *value,
+                    const int64_t *slot_mapping, void *key_cache, void *value_cache,
+                    const int32_t *block_tables, int max_blocks_per_seq, const int32_t *context_lens,
+                    int max_context_len, int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                    int block_size, int num_blocks, float scale, pa_dtype kv_dtype, void *workspace,
+                    size_t workspace_bytes, int32_t *status, pa_stream_t stream) {
+    int rc = check_attention(out, out_dtype, query, key_cache, value_cache, block_tables,
+                             max_blocks_per_seq, context_lens, max_context_len, num_seqs,
+                             num_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,
+                             kv_dtype);
+    if (rc != PA_OK || num_seqs == 0) return rc;
+    if (!key || !value || !slot_mapping) return PA_ERR_INVALID_ARG;
+    if (!aligned(key, 16) || !aligned(value, 16) || !aligned(slot_mapping, 8) || !aligned(status, 4))
+        return PA_ERR_INVALID_ARG;
+    if (!workspace || !aligned(workspace, 16)) return PA_ERR_WORKSPACE;
+    pa::DecodeArgs a{out,          out_dtype,      query,     key_cache,    value_cache,
+                     block_tables, max_blocks_per_seq, context_lens, max_context_len,
+                     num_seqs,     num_heads,      num_kv_heads, head_dim,  block_size,
+                     num_blocks,   scale,          kv_dtype,  workspace,    workspace_bytes,
+                     status,       reinterpret_cast<cudaStream_t>(stream)};
+    a.new_key = key;
+    a.new_value = value;
+    a.slot_mapping = slot_mapping;
+    return pa::launch_decode(a);
+}
+
 // The rotary-embedding arguments shared by the two fused entry points.
 static int check_rope(const pa_rope *rope, int head_dim) {
     if (!rope || !rope->freqs || !aligned(rope->freqs, 4)) return PA_ERR_INVALID_ARG;
