@@ -240,6 +240,13 @@ class DecodeStep:
                           self.case.scale, workspace=self.ws)
 
     def step(self):
+        """The decode step: every sequence's new token written to its slot and attended, in
+        one call (pa_decode_write)."""
+        self.pa.pa_decode_write(self.out, self.q, self.nk, self.nv, self.slots, self.kc, self.vc, self.bt,
+                                self.cl, self.max_ctx, self.case.scale, workspace=self.ws)
+
+    def step_separate(self):
+        """The same step as two calls: pa_reshape_and_cache, then pa_decode."""
         self.reshape()
         self.decode()
 
@@ -248,9 +255,8 @@ class DecodeStep:
         step through the public API on the device copies, one D2H copy of the output."""
         self.d_in.copy_(self.h_in, non_blocking=True)
         v = self.e2e_views
-        self.pa.pa_reshape_and_cache(v["nk"], v["nv"], self.kc, self.vc, v["slots"])
-        self.pa.pa_decode(self.out, v["q"], self.kc, self.vc, v["bt"], v["cl"], self.max_ctx,
-                          self.case.scale, workspace=self.ws)
+        self.pa.pa_decode_write(self.out, v["q"], v["nk"], v["nv"], v["slots"], self.kc, self.vc, v["bt"],
+                                v["cl"], self.max_ctx, self.case.scale, workspace=self.ws)
         self.h_out.copy_(self.out, non_blocking=True)
 
     def h2d_bytes(self):
@@ -260,11 +266,11 @@ class DecodeStep:
         return self.h_out.numel() * self.h_out.element_size()
 
     def launches_per_step(self):
-        # pa_reshape_and_cache: 1 kernel; pa_decode: split + reduce, and a plan kernel
-        # first when there are 2048 or more (kv-head group, sequence) segments
+        # pa_decode_write: split (with the cache write) + reduce, and a plan kernel first
+        # when there are 2048 or more (kv-head group, sequence) segments
         c = self.case
         segments = max(1, c.num_kv_heads // 8) * c.num_seqs
-        return 3 + (1 if segments >= 2048 else 0)
+        return 2 + (1 if segments >= 2048 else 0)
 
 
 class PrefillStep:
@@ -442,12 +448,14 @@ def gpu_arm(args, rank, world, dist_on):
     dec_ms, _ = time_steps(st.decode, args.steps, flush, dist_on)
     with ClockSampler(device.index) as clocks:
         step_ms, wall = time_steps(st.step, args.steps, flush, dist_on)
+    sep_ms, _ = time_steps(st.step_separate, max(3, args.steps // 4), flush, dist_on)
     for _ in range(3):
         st.e2e_step()
     torch.cuda.synchronize()
     e2e_ms, _ = time_steps(st.e2e_step, max(3, args.steps // 4), flush, dist_on)
 
     ms_step = _max_over_ranks(statistics.median(step_ms), dist_on)
+    ms_sep = _max_over_ranks(statistics.median(sep_ms), dist_on)
     ms_dec = _max_over_ranks(statistics.median(dec_ms), dist_on)
     ms_e2e = _max_over_ranks(statistics.median(e2e_ms), dist_on)
     value = world * byts["step"] / (ms_step * 1e-3) / 1e9
@@ -488,8 +496,11 @@ def gpu_arm(args, rank, world, dist_on):
             "kv_bytes_per_step": byts["kv"],
             "l2": "inputs larger than L2, and L2 flushed before each timed step (256 MB write, then 256 MB read of another buffer, outside the timed events)",
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+            "step": "pa_decode_write: every sequence's new token written to its cache slot and decode attention, one call",
         },
         "seq_steps_per_s": round(world * case.num_seqs / (ms_step * 1e-3), 1),
+        "step_as_two_calls": {"ms": round(ms_sep, 5), "GB/s": round(world * byts["step"] / (ms_sep * 1e-3) / 1e9, 2),
+                              "calls": "pa_reshape_and_cache, then pa_decode"},
         "pct_of_peak": {"measured_hbm": round(100 * value / world / hbm_peak, 1),
                         "nominal_8TBs": round(100 * value / world / NOMINAL_HBM_GBS, 1)},
         "roofline": {
@@ -507,7 +518,8 @@ def gpu_arm(args, rank, world, dist_on):
         "e2e": {"value": round(e2e_gbs, 2), "unit": "GB/s", "ms_per_step": round(ms_e2e, 5),
                 "h2d_bytes_per_step": st.h2d_bytes(), "d2h_bytes_per_step": st.d2h_bytes()},
         "gpu_launches": args.steps * st.launches_per_step(),
-        "step_ms": {"step": step_stats(step_ms), "pa_decode": step_stats(dec_ms), "e2e": step_stats(e2e_ms),
+        "step_ms": {"step": step_stats(step_ms), "step_as_two_calls": step_stats(sep_ms),
+                    "pa_decode": step_stats(dec_ms), "e2e": step_stats(e2e_ms),
                     "statistic": "median of the per-step CUDA-event times (p10 / p90 / mean beside it)"},
         "clocks": clocks.summary(),
         "timed_region_s": round(wall, 3),

@@ -42,9 +42,10 @@ int pa_engine_upload(void *dev_batch, const void *host_batch, const pa_sched_off
 
 /*
  * pa_engine_attend -- the paged-attention work of one planned step, on stream, in order:
- * pa_copy_blocks over the step's copy pairs (when it has any), pa_reshape_and_cache of k and
- * v through the step's slot mapping, then pa_decode (a decode step, with `workspace` as for
- * pa_decode) or pa_prefill_chunk (a prefill step) of q into out.
+ * pa_copy_blocks over the step's copy pairs (when it has any), then for a decode step
+ * pa_decode_write (its one new token per sequence written through the slot mapping and
+ * attended, with `workspace` as for pa_decode), for a prefill step pa_reshape_and_cache of k
+ * and v through the slot mapping and pa_prefill_chunk of q into out.
  *
  *   batch, offsets  the step as pa_sched_step_packed described it
  *   dev_batch       the uploaded device copy of the step (pa_engine_upload)

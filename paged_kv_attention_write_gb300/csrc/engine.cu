@@ -32,6 +32,11 @@ extern "C" int pa_engine_attend(const pa_engine_cache *c, const pa_sched_batch *
         rc = pa_copy_blocks(c->key_cache, c->value_cache, pairs, b->num_copy_pairs, c->num_kv_heads, c->head_dim,
                             c->block_size, c->num_blocks, c->kv_dtype, status, stream);
     if (rc != PA_OK) return rc;
+    if (b->kind == PA_SCHED_DECODE && b->num_tokens == b->num_seqs)  // one new token per sequence, at its end
+        return pa_decode_write(out, out_dtype, q, k, v, slots, c->key_cache, c->value_cache, bt, b->table_width, cl,
+                               b->max_context_len, b->num_seqs, c->num_heads, c->num_kv_heads, c->head_dim,
+                               c->block_size, c->num_blocks, c->scale, c->kv_dtype, workspace, workspace_bytes,
+                               status, stream);
     rc = pa_reshape_and_cache(k, v, c->key_cache, c->value_cache, slots, b->num_tokens, c->num_kv_heads,
                               c->head_dim, c->block_size, c->num_blocks, c->kv_dtype, status, stream);
     if (rc != PA_OK) return rc;
