@@ -811,6 +811,11 @@ def secondary_measurements(device, flush, hbm_peak, tc_peak, peak_kind):
     t = statistics.median(ms)
     rb = nk.numel() * nk.element_size() * 4 + sl.numel() * 8
     res["reshape_and_cache_2048_tokens"] = {"ms": round(t, 5), "GB/s": round(rb / (t * 1e-3) / 1e9, 1)}
+    # the same call on 8 tokens: the floor of a launch timed this way (events around one call
+    # after the L2 flush), next to which the 2048 tokens' 16.8 MB are measured
+    ms, _ = time_steps(lambda: pa.pa_reshape_and_cache(nk[:8], nv[:8], kc, vc, sl[:8]), 50, flush, False)
+    res["reshape_and_cache_8_tokens"] = {"ms": round(statistics.median(ms), 5),
+                                         "note": "launch floor under the same timing"}
     del kc, vc
     res["rope"] = rope_measurement(device, flush, hbm_peak)
     res["mixed_batch"] = mixed_batch_measurement(device, flush, hbm_peak, tc_peak)
