@@ -70,6 +70,16 @@ def oracle_step(case, oracle):
     return ref, kc, vc
 
 
+def oracle_step_pools(case, oracle):
+    """The oracle's pools after the case's block copies and cache write (no attention)."""
+    kc = case.key_cache.clone()
+    vc = case.value_cache.clone()
+    if case.block_mapping is not None:
+        oracle.copy_blocks(kc, vc, case.block_mapping, case.block_size)
+    oracle.reshape_and_cache(case.new_key, case.new_value, kc, vc, case.slot_mapping, case.block_size)
+    return None, kc, vc
+
+
 def attention_errors(got: torch.Tensor, ref: np.ndarray):
     g = got.float().numpy().astype(np.float64)
     r = ref.astype(np.float32).astype(np.float64)

@@ -114,3 +114,32 @@ def test_reshape_copy_prefill_reject_bad_arguments(lib):
     no_qsl = list(base)
     no_qsl[3] = None
     assert h(*no_qsl) == -1
+
+
+def _decode_write(lib, **over):
+    args = dict(out=FAKE, out_dtype=0, query=FAKE, key=FAKE, value=FAKE, slots=FAKE, kc=FAKE, vc=FAKE, bt=FAKE,
+                mbps=4, cl=FAKE, maxctx=100, S=2, Hq=32, Hkv=8, D=128, bs=32, NB=16, scale=0.088, kvdt=2,
+                ws=FAKE, wsb=1 << 30, status=None, stream=None)
+    args.update(over)
+    f = lib.pa_decode_write
+    vp, i, fl, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    f.argtypes = [vp, i, vp, vp, vp, vp, vp, vp, vp, i, vp, i, i, i, i, i, i, i, fl, i, vp, sz, vp, vp]
+    return f(*args.values())
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(key=None), -1), (dict(value=None), -1), (dict(slots=None), -1), (dict(key=FAKE + 8), -1),
+    (dict(slots=FAKE + 4), -1), (dict(D=96), -2), (dict(ws=None), -3), (dict(query=None), -1),
+])
+def test_decode_write_rejects_bad_arguments(lib, over, code):
+    assert _decode_write(lib, **over) == code
+
+
+def test_decode_write_and_prefill_with_nothing_to_do_are_noops(lib):
+    assert _decode_write(lib, S=0, query=None, out=None, key=None, value=None, slots=None) == 0
+    vp, i, fl = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    h = lib.pa_prefill_chunk
+    h.argtypes = [vp, i, vp, vp, i, i, vp, vp, vp, i, vp, i, i, i, i, i, i, i, fl, i, vp, vp]
+    # no sequences, and no query tokens: nothing is read or launched
+    assert h(None, 0, None, None, 0, 0, FAKE, FAKE, FAKE, 8, FAKE, 256, 0, 32, 8, 128, 32, 16, 0.088, 2,
+             None, None) == 0

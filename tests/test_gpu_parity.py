@@ -8,7 +8,7 @@ import pytest
 import torch
 
 import workloads
-from paged_steps import (assert_attention_close, bits, check_case, gpu_step, oracle_step)
+from paged_steps import (assert_attention_close, bits, check_case, gpu_step, oracle_step, oracle_step_pools)
 
 pytestmark = pytest.mark.gpu
 
@@ -204,6 +204,13 @@ def test_decode_aliased_block_tables(oracle_mod):
     check_case(case, oracle_mod)
 
 
+def test_decode_one_sequence_of_128k_tokens(oracle_mod):
+    """The largest single context of the tests: 131,072 tokens (4,096 blocks of 32), one
+    sequence split into one piece per CTA, so the reduce merges ~150 pieces in batches."""
+    case = workloads.make_decode_case("128k", [131071], 32, 32, 8, 128, torch.bfloat16, 128)
+    check_case(case, oracle_mod)
+
+
 # ----------------------------------------------------------------------------- prefill shapes and edges
 
 @pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16], ids=["fp16", "bf16"])
@@ -286,6 +293,35 @@ def test_mixed_batch_decode_rows_match_alone_and_decode():
     torch.cuda.synchronize()
     assert torch.equal(out_mix[:nd], alone.cpu())
     assert (dec.cpu() - out_mix[:nd]).abs().max().item() < 5e-3
+
+
+def test_prefill_long_prefix_large_chunks_sampled_rows(oracle_mod):
+    """Two 2048-token chunks, one over a 16,384-token prefix (the unit of ~144 key tiles), one
+    fresh: the whole launch on the GPU, and 48 rows per sequence -- the chunk's first and last
+    rows, rows at 128-key tile edges, the rest random -- against the oracle, each sampled row
+    as a one-row query over keys 0 .. its position (the causal definition)."""
+    import paged_kv_attention_write_gb300 as pa
+    case = workloads.make_prefill_case("long-prefix", [16384, 0], [2048, 2048], 16, 32, 8, 128,
+                                       torch.bfloat16, 31)
+    out, *_ , status = gpu_step(case)
+    assert status == 0
+    _, okc, ovc = oracle_step_pools(case, oracle_mod)
+    rng = np.random.default_rng(31)
+    qsl = case.query_start_loc.tolist()
+    rows, bts, cls = [], [], []
+    for s_ in range(case.num_seqs):
+        Lq = qsl[s_ + 1] - qsl[s_]
+        P = int(case.context_lens[s_]) - Lq
+        pick = {0, 1, Lq - 1, Lq - 2} | {r for r in (127, 128, 255, 256, 1023, 1024) if r < Lq}
+        pick |= set(int(x) for x in rng.integers(0, Lq, size=48 - len(pick)))
+        for r in sorted(pick)[:48]:
+            rows.append(qsl[s_] + r)
+            bts.append(case.block_tables[s_])
+            cls.append(P + r + 1)
+    idx = torch.tensor(rows)
+    ref = oracle_mod.paged_attention(case.query[idx], torch.arange(len(rows) + 1, dtype=torch.int32), okc, ovc,
+                                     torch.stack(bts), torch.tensor(cls, dtype=torch.int32), case.scale)
+    assert_attention_close(out[idx], ref)
 
 
 def test_prefill_single_row_matches_decode(oracle_mod):
