@@ -18,14 +18,17 @@ def _need_gpu(cuda_ok):
     yield
 
 
-def _both(case, pad=()):
-    """(separate out, fused out, separate pools, fused pools) for a decode case whose new tokens
-    are not yet in the pools; the sequences in `pad` get slot -1 (nothing written)."""
+def _both(case, pad=(), past=(), want_status=0):
+    """[(out, key pool, value pool) of the two calls, the same of the fused call] for a decode
+    case whose new tokens are not yet in the pools; the sequences in `pad` get slot -1 (nothing
+    written), those in `past` a slot past the pool (reported, nothing written)."""
     import paged_kv_attention_write_gb300 as pa
     dev = "cuda"
     slots = case.slot_mapping.clone()
     for s in pad:
         slots[s] = -1
+    for s in past:
+        slots[s] = case.key_cache.shape[0] * case.block_size + 3 + s
     q, nk, nv = case.query.to(dev), case.new_key.to(dev), case.new_value.to(dev)
     bt, cl, sl = case.block_tables.to(dev), case.context_lens.to(dev), slots.to(dev)
     S, Hq, D = case.query.shape
@@ -43,7 +46,7 @@ def _both(case, pad=()):
             pa.pa_reshape_and_cache(nk, nv, kc, vc, sl, status=status)
             pa.pa_decode(out, q, kc, vc, bt, cl, mcl, case.scale, workspace=ws, status=status)
         torch.cuda.synchronize()
-        assert status.item() == 0
+        assert status.item() == want_status
         res.append((out.cpu(), kc.cpu(), vc.cpu()))
     return res
 
@@ -94,3 +97,12 @@ def test_decode_write_against_oracle(oracle_mod):
     ref, okc, ovc = oracle_step(case, oracle_mod)
     assert_attention_close(res[1][0], ref)
     assert torch.equal(bits(res[1][1]), bits(okc)) and torch.equal(bits(res[1][2]), bits(ovc))
+
+
+def test_decode_write_reports_a_slot_past_the_pool():
+    """A slot past the pool is reported (PA_DEVERR_SLOT) and not written by either path; the
+    attention then reads what the cache holds there, the same in both."""
+    rng = np.random.default_rng(9)
+    lens = [int(x) for x in rng.integers(1, 2000, size=12)]
+    case = workloads.make_decode_case("dwbad", lens, 16, 32, 8, 128, torch.bfloat16, 9)
+    _same(_both(case, past=(2, 7), want_status=1))
