@@ -137,6 +137,10 @@ size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads, i
  *                  64-bit tag), its contents are clobbered, and two calls in
  *                  flight must not share it
  *
+ * A call made while `stream` is being captured into a CUDA graph is replayable: the
+ * merge of the split context then waits for the whole first pass instead of the
+ * per-call tags (a replay repeats the captured tag), a few microseconds slower.
+ *
  *   out[s][h] = sum_j softmax_j(scale * q[s][h] . k_j) v_j over j < context_lens[s];
  *   a sequence with context length 0 gets an all-zero row.
  * Accumulation is fp32; the result does not depend on the split.

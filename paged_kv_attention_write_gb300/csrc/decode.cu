@@ -88,6 +88,9 @@ int launch_decode(const DecodeArgs &a) {
     prm.part_o = reinterpret_cast<float *>(ws + L.o);
     prm.tags = reinterpret_cast<unsigned long long *>(ws + L.tag);
     prm.launch_tag = next_launch_tag();
+    cudaStreamCaptureStatus capture = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(a.stream, &capture) != cudaSuccess) return PA_ERR_CUDA;
+    prm.tagged = capture == cudaStreamCaptureStatusNone ? 1 : 0;
     prm.max_blocks_per_seq = a.max_blocks_per_seq;
     prm.num_seqs = a.num_seqs;
     prm.num_heads = a.num_heads;

@@ -31,7 +31,9 @@
 // once their data is visible, and a reduce CTA -- small enough to be resident beside a
 // split CTA -- waits (acquire, bounded in time) for the tags of its segment's pieces.
 // It waits for the split grid only before it exits, so that the reduce grid still ends
-// after every output the split kernel writes directly.
+// after every output the split kernel writes directly.  A launch made while its stream is
+// captured into a CUDA graph merges after the end of the split grid instead: every replay
+// of the graph carries the same tag, which the previous replay left in the workspace.
 //
 // Split kernel, per CTA: one producer warp issues 3-D TMA loads of whole
 // [tokens][HG heads][D] boxes of K and V (one box per block piece, taken
@@ -65,6 +67,8 @@ struct DecodeParams {
     // for segment k is written; each holds launch_tag once its data is visible
     unsigned long long *tags;
     unsigned long long launch_tag;
+    int tagged;           // the reduce waits for tags (else for the end of the split grid: a
+                          // launch captured into a CUDA graph replays with one fixed tag)
     int scan_in_split;    // the split kernel's CTA 0 writes the segment table (else the plan kernel)
     int max_blocks_per_seq, num_seqs, num_heads, num_kv_heads, block_size, num_blocks;
     int max_context_len, head_dim;
@@ -987,10 +991,10 @@ __global__ void __launch_bounds__(D / 2 * kReduceHeads) decode_reduce_kernel(con
     const int tid = threadIdx.y * blockDim.x + threadIdx.x;
     const int k = blockIdx.x, hl = blockIdx.y * blockDim.y + threadIdx.y, d = threadIdx.x * 2;
     const int S = p.num_seqs, K = p.num_groups * S;
-    if (p.scan_in_split) {
+    if (p.tagged && p.scan_in_split) {
         if (tid == 0) ready = wait_tag(p.tags, p.launch_tag, p.status);
     } else {
-        pdl_wait_previous();  // the plan kernel wrote the table before the split kernel began
+        pdl_wait_previous();  // the split grid has ended (or, tagged, the plan kernel before it)
         if (tid == 0) ready = 1;
     }
     __syncthreads();
@@ -1007,7 +1011,7 @@ __global__ void __launch_bounds__(D / 2 * kReduceHeads) decode_reduce_kernel(con
     }
     if (n > 0) {  // the same in every thread of the CTA
         __syncthreads();  // every thread has read `ready`
-        if (tid < 32) {   // lane j waits for the pieces j, j + 32, ...
+        if (tid < 32 && p.tagged) {  // lane j waits for the pieces j, j + 32, ...
             bool all = true;
             for (int j = tid; j < n; j += 32) all = wait_tag(p.tags + 1 + c_lo + k + j, p.launch_tag, p.status) && all;
             all = __all_sync(kFullMask, all);
