@@ -19,9 +19,14 @@ struct Layout {
     size_t seg, k0, m, l, o, tag, total;
 };
 
+// Query slices per kv head: two when a kv head has eight query heads (each consumer warp then
+// holds four of them), else one.
+int query_slices(int num_heads, int num_kv_heads) { return num_heads / num_kv_heads > 4 ? 2 : 1; }
+
 Layout layout(int num_seqs, int num_heads, int num_kv_heads, int head_dim, int sms) {
     Layout L{};
-    L.HG = num_kv_heads < 8 ? num_kv_heads : 8;
+    const int hg_max = 8 / query_slices(num_heads, num_kv_heads);  // kv heads a stage holds
+    L.HG = num_kv_heads < hg_max ? num_kv_heads : hg_max;
     L.groups = num_kv_heads / L.HG;
     L.HGq = L.HG * (num_heads / num_kv_heads);
     L.K = L.groups * num_seqs;
@@ -119,8 +124,9 @@ int launch_decode(const DecodeArgs &a) {
     // tensor maps with the largest box the shape can use and re-encode if smaller.
     const int eb = a.kv_dtype == PA_F32 ? 4 : 2;
     const int G = a.num_heads / a.num_kv_heads;
-    const int nt = (a.head_dim * eb <= 256 && G <= 4) ? 16 : 8;  // DecodeShape::NT
-    const int tu = nt * (kConsumerWarps / L.HG);
+    const int qs = query_slices(a.num_heads, a.num_kv_heads);
+    const int nt = a.head_dim * eb <= 256 ? 16 : 8;  // DecodeShape::NT (at most four heads per warp)
+    const int tu = nt * (kConsumerWarps / (L.HG * qs));
     const int rows = a.block_size < tu ? a.block_size : tu;
     const int64_t pool_rows = (int64_t)a.num_blocks * a.block_size;
     if (pool_rows <= 0 || pool_rows > INT32_MAX) return PA_ERR_INVALID_ARG;

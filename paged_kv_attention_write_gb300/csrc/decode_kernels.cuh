@@ -39,7 +39,9 @@
 // [tokens][HG heads][D] boxes of K and V (one box per block piece, taken
 // through the block table) into an NSTAGE-deep shared-memory ring guarded by
 // full/empty mbarriers; eight consumer warps each own one kv head (and a
-// token slice of the stage when HG < 8) and the G query heads that read it.
+// token slice of the stage when HG * QS < 8) and G of the query heads that read it:
+// all of them (QS = 1) while a kv head has at most four, else half (QS = 2 query slices,
+// two warps reading the same K/V rows), so that a lane's state never exceeds four heads.
 // Lanes own 16-byte slices of the head dimension; the q.k partial dot
 // products of a batch of tokens are reduce-scattered across a token row's
 // lanes so that every lane finishes with whole scores; the online softmax
@@ -109,7 +111,7 @@ constexpr int kPlanThreads = 1024;
 constexpr int kSegSmem = 2048;  // segments whose scan the split kernel keeps in shared memory
 constexpr float kRescaleLog2 = 8.f;  // lazy softmax: rescale when a score exceeds the reference by 2^8
 
-template <class T, int D, int G>
+template <class T, int D, int G, int QS = 1>
 struct DecodeShape {
     static constexpr int EPV = T::kPerVec;            // elements per 16-byte vector
     static constexpr int LPT = D / EPV;               // lanes covering one token row
@@ -122,7 +124,7 @@ struct DecodeShape {
     static constexpr int R = NV >= LPT ? NV / LPT : 1;  // whole scores per lane
     static constexpr int TOKEN_BITS = NTG >= 16 ? 4 : NTG >= 8 ? 3 : NTG >= 4 ? 2 : NTG >= 2 ? 1 : 0;
     static_assert((1 << TOKEN_BITS) == NTG && NTG <= LPT, "token slots: a power of two, at most LPT");
-    static constexpr int STAGE_ROWS = NT * kConsumerWarps;
+    static constexpr int STAGE_ROWS = NT * kConsumerWarps / QS;  // (token, kv head) rows of a stage
     static constexpr int KV_BYTES = STAGE_ROWS * ROW_BYTES;  // K (and V) bytes per stage
     static constexpr int RED_BYTES = kConsumerWarps * G * (D + 2) * 4;
     static constexpr int SC_BYTES = kConsumerWarps * NT * G * 4;
@@ -436,11 +438,12 @@ __device__ void publish_scan(const DecodeParams &p, const int *sseg, int K, int 
 
 // ------------------------------------------------------------------------------ split kernel
 
-template <class T, int D, int G, bool ROPE, bool WRITE>
+template <class T, int D, int G, int QS, bool ROPE, bool WRITE>
 __global__ void __launch_bounds__(kDecodeThreads, 1)
 decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                     const DecodeParams p) {
-    using Sh = DecodeShape<T, D, G>;
+    using Sh = DecodeShape<T, D, G, QS>;
+    constexpr int GQ = G * QS;  // query heads per kv head (this warp holds G of them)
     constexpr int EPV = Sh::EPV, LPT = Sh::LPT, TPW = Sh::TPW, NT = Sh::NT, NTG = Sh::NTG;
     constexpr int NV = Sh::NV, NSTAGE = Sh::NSTAGE, KVB = Sh::KV_BYTES, ROWB = Sh::ROW_BYTES;
     constexpr int NW = kConsumerWarps;
@@ -479,7 +482,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
     const int K = p.num_groups * S;
     const int c = blockIdx.x;
     const int cap = min(p.max_blocks_per_seq * p.block_size, p.max_context_len);
-    const int HG = p.heads_per_group, HGq = HG * G, TU = p.unit_tokens;
+    const int HG = p.heads_per_group, HGq = HG * GQ, TU = p.unit_tokens;
     const bool fused = K < kSegSmem;
     const int *segs = fused ? sseg : p.seg_start;
     if (fused) {
@@ -555,8 +558,9 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
     }
 
     // ============================================================ consumers
-    const int h = warp % HG;     // kv head within the group
-    const int sb = warp / HG;    // token slice of the stage
+    const int h = warp % HG;          // kv head within the group
+    const int qs = (warp / HG) % QS;  // query slice: heads h * GQ + qs * G .. + G - 1 of the group
+    const int sb = warp / (HG * QS);  // token slice of the stage
     const int grp = lane / LPT, r = lane % LPT;
     float *wsc = scores + warp * NT * G;
     // After the reduce-scatter, lane r holds whole scores of one token of its slice,
@@ -587,10 +591,10 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
             l_lane[u] = 0.f;
         }
     };
-    // This lane's 16-byte slices of the G query rows of (sequence s, head group hg).
+    // This lane's 16-byte slices of the warp's G query rows of (sequence s, head group hg).
     auto q_global = [&](int s, int hg, uint4 (&raw)[G]) {
         const typename T::storage *qp = static_cast<const typename T::storage *>(p.query) +
-                                        ((int64_t)s * p.num_heads + hg * HGq + h * G) * D + r * EPV;
+                                        ((int64_t)s * p.num_heads + hg * HGq + h * GQ + qs * G) * D + r * EPV;
 #pragma unroll
         for (int hh = 0; hh < G; ++hh) raw[hh] = *reinterpret_cast<const uint4 *>(qp + hh * D);
     };
@@ -598,12 +602,12 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
     // flush then needs no shared memory) each warp copies its rows into its own slice of
     // red_o with cp.async while it streams the segment's last unit, so that the switch
     // waits for no global load.
-    const bool q_prefetch = G <= 4 && HG == NW;
+    const bool q_prefetch = G <= 4 && HG * QS == NW;
     const uint32_t q_slot = smem_u32(red_o) + (uint32_t)(warp * G * D * (int)sizeof(typename T::storage));
     auto q_prefetch_issue = [&](int s, int hg) {
         if (grp == 0) {
             const typename T::storage *qp = static_cast<const typename T::storage *>(p.query) +
-                                            ((int64_t)s * p.num_heads + hg * HGq + h * G) * D + r * EPV;
+                                            ((int64_t)s * p.num_heads + hg * HGq + h * GQ + qs * G) * D + r * EPV;
 #pragma unroll
             for (int hh = 0; hh < G; ++hh)
                 asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
@@ -781,12 +785,12 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
             for (int o = 1; o < 32; o <<= 1) v += __shfl_xor_sync(kFullMask, v, o);
             lsum[hh] = v;
         }
-        const int s = k % S, hg = k / S, nsub = NW / HG;
-        if (G <= 4 && nsub == 1) {  // every warp holds whole rows of its kv head: write from registers
+        const int s = k % S, hg = k / S, nsub = NW / (HG * QS);
+        if (G <= 4 && nsub == 1) {  // every warp holds whole rows of its heads: write from registers
             if (grp == 0) {
 #pragma unroll
                 for (int hh = 0; hh < G; ++hh) {
-                    const int hl = h * G + hh;
+                    const int hl = h * GQ + qs * G + hh;
                     if (whole) {
                         const float inv = 1.f / lsum[hh];
                         const int64_t o0 = ((int64_t)s * p.num_heads + hg * HGq + hl) * D + r * EPV;
@@ -825,12 +829,12 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
         named_barrier(1, NW * 32);
         for (int idx = threadIdx.x; idx < HGq * (D / 2); idx += NW * 32) {
             const int hl = idx / (D / 2), d = (idx % (D / 2)) * 2;
-            const int hk = hl / G, hh = hl % G;
-            float M = -INFINITY;
-            for (int j = 0; j < nsub; ++j) M = fmaxf(M, red_m[(j * HG + hk) * G + hh]);
+            const int hk = hl / GQ, hq = hl % GQ / G, hh = hl % G;
+            float M = -INFINITY;  // warp of token slice j: j * HG * QS + hq * HG + hk
+            for (int j = 0; j < nsub; ++j) M = fmaxf(M, red_m[((j * QS + hq) * HG + hk) * G + hh]);
             float L = 0.f, o0 = 0.f, o1 = 0.f;
             for (int j = 0; j < nsub; ++j) {
-                const int w = j * HG + hk;
+                const int w = (j * QS + hq) * HG + hk;
                 const float f = fast_exp2(red_m[w * G + hh] - M);  // 0 for a slice without tokens
                 L = fmaf(red_l[w * G + hh], f, L);
                 o0 = fmaf(red_o[(w * G + hh) * D + d], f, o0);
@@ -881,8 +885,10 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
                 using ST = typename T::storage;
                 new_k = ldg_stream(reinterpret_cast<const uint4 *>(static_cast<const ST *>(p.new_key) + src));
                 new_v = ldg_stream(reinterpret_cast<const uint4 *>(static_cast<const ST *>(p.new_value) + src));
-                *reinterpret_cast<uint4 *>(static_cast<ST *>(p.key_cache_w) + dst) = new_k;
-                *reinterpret_cast<uint4 *>(static_cast<ST *>(p.value_cache_w) + dst) = new_v;
+                if (qs == 0) {  // both query slices patch their stage; one stores to the cache
+                    *reinterpret_cast<uint4 *>(static_cast<ST *>(p.key_cache_w) + dst) = new_k;
+                    *reinterpret_cast<uint4 *>(static_cast<ST *>(p.value_cache_w) + dst) = new_v;
+                }
             }
         }
     };
@@ -1057,21 +1063,21 @@ __global__ void __launch_bounds__(D / 2 * kReduceHeads) decode_reduce_kernel(con
     pdl_wait_previous();  // this grid ends after the split kernel (whose whole segments it does not await)
 }
 
-template <class T, int D, int G, bool ROPE, bool WRITE>
+template <class T, int D, int G, int QS, bool ROPE, bool WRITE>
 int launch_typed(DecodeParams prm, const CUtensorMap &km, const CUtensorMap &vm, cudaStream_t st) {
-    using Sh = DecodeShape<T, D, G>;
+    using Sh = DecodeShape<T, D, G, QS>;
     static std::atomic<int> smem_ready[kMaxDevices];  // per device: shared-memory limit raised
-    prm.unit_tokens = Sh::NT * (kConsumerWarps / prm.heads_per_group);
+    prm.unit_tokens = Sh::NT * (kConsumerWarps / (prm.heads_per_group * QS));
     prm.box_rows = prm.block_size < prm.unit_tokens ? prm.block_size : prm.unit_tokens;
     const bool fused = prm.num_groups * prm.num_seqs < kSegSmem;  // scan inside the split kernel
     prm.scan_in_split = fused ? 1 : 0;
     // reduce: heads per CTA, as many as keep about 128 CTAs (one wave)
-    const int K = prm.num_groups * prm.num_seqs, HGq = prm.heads_per_group * G;
+    const int K = prm.num_groups * prm.num_seqs, HGq = prm.heads_per_group * G * QS;
     int rh = kReduceHeads;
     while (rh > 1 && (int64_t)K * ((HGq + rh - 1) / rh) < 128) rh >>= 1;
     if ((!fused &&
          launch_pdl(decode_plan_kernel, dim3(1), dim3(kPlanThreads), 0, st, prm) != cudaSuccess) ||
-        launch_pdl_smem(decode_split_kernel<T, D, G, ROPE, WRITE>, smem_ready, dim3(prm.grid), dim3(kDecodeThreads),
+        launch_pdl_smem(decode_split_kernel<T, D, G, QS, ROPE, WRITE>, smem_ready, dim3(prm.grid), dim3(kDecodeThreads),
                         Sh::SMEM, st, km, vm, prm) != cudaSuccess ||
         launch_pdl(decode_reduce_kernel<D>, dim3(K, (HGq + rh - 1) / rh), dim3(D / 2, rh), 0, st, prm, HGq) !=
             cudaSuccess)
@@ -1083,10 +1089,10 @@ template <class T, int D, bool ROPE, bool WRITE>
 int dispatch_g(const DecodeParams &prm, int G, const CUtensorMap &km, const CUtensorMap &vm,
                cudaStream_t st) {
     switch (G) {
-        case 1: return launch_typed<T, D, 1, ROPE, WRITE>(prm, km, vm, st);
-        case 2: return launch_typed<T, D, 2, ROPE, WRITE>(prm, km, vm, st);
-        case 4: return launch_typed<T, D, 4, ROPE, WRITE>(prm, km, vm, st);
-        case 8: return launch_typed<T, D, 8, ROPE, WRITE>(prm, km, vm, st);
+        case 1: return launch_typed<T, D, 1, 1, ROPE, WRITE>(prm, km, vm, st);
+        case 2: return launch_typed<T, D, 2, 1, ROPE, WRITE>(prm, km, vm, st);
+        case 4: return launch_typed<T, D, 4, 1, ROPE, WRITE>(prm, km, vm, st);
+        case 8: return launch_typed<T, D, 4, 2, ROPE, WRITE>(prm, km, vm, st);  // two query slices
         default: return PA_ERR_UNSUPPORTED;
     }
 }
