@@ -858,6 +858,34 @@ def secondary_measurements(device, flush, hbm_peak, tc_peak, peak_kind):
                 "seq_steps_per_s": round(case.num_seqs / t * 1e3, 1)}
             del st
             torch.cuda.empty_cache()
+    res["decode_group_sizes"] = group_size_measurement(device, flush, hbm_peak)
+    return res
+
+
+def group_size_measurement(device, flush, hbm_peak):
+    """pa_decode on one long-context cache (8 kv heads) with 1, 2, 4 and 8 query heads per kv
+    head: the same K/V bytes, a fresh random query of each width."""
+    import paged_kv_attention_write_gb300 as pa
+    case = workloads.gqa_decode(8)
+    st = DecodeStep(case, device)
+    st.reshape()
+    S, D = case.num_seqs, case.head_dim
+    g = torch.Generator(device=device).manual_seed(8)
+    res = {"workload": case.name, "note": "query heads = 8 x G; K/V bytes identical across G"}
+    for G in (1, 2, 4, 8):
+        q = torch.randn((S, 8 * G, D), generator=g, device=device).to(case.dtype)
+        out = torch.empty((S, 8 * G, D), dtype=torch.float32, device=device)
+
+        def dec():
+            pa.pa_decode(out, q, st.kc, st.vc, st.bt, st.cl, st.max_ctx, case.scale, workspace=st.ws)
+        for _ in range(3):
+            dec()
+        ms, _ = time_steps(dec, 30, flush, False)
+        t = statistics.median(ms)
+        b = decode_bytes(case)["kv"] + S * 8 * G * D * (2 + 4)
+        res[f"G{G}"] = {"ms": round(t, 5), "GB/s": round(b / t / 1e6, 1), "frac_hbm": round(b / t / 1e6 / hbm_peak, 4)}
+    del st
+    torch.cuda.empty_cache()
     return res
 
 

@@ -35,7 +35,7 @@ import torch
 
 __all__ = [
     "PagedCase", "make_decode_case", "make_prefill_case", "tiny_decode", "decode_batch",
-    "long_decode", "prefill_chunk", "stress_decode", "mixed_batch", "WORKLOADS",
+    "long_decode", "prefill_chunk", "stress_decode", "mixed_batch", "gqa_decode", "WORKLOADS",
 ]
 
 
@@ -257,6 +257,16 @@ def prefill_chunk(seed: int = 4) -> PagedCase:
                              [0, 1024, 2048, 3584], [512] * 4, 16, 32, 8, 128, torch.bfloat16, seed)
 
 
+def gqa_decode(group: int = 8, seed: int = 7) -> PagedCase:
+    """The long-context shape with `group` query heads per kv head (8 kv heads): 8 sequences,
+    cached lengths uniform in [16384, 32768], block 32, D 128, bf16.  Eight query heads per kv
+    head is the grouping of the larger GQA models."""
+    rng = np.random.default_rng(1000 + seed)
+    L = rng.integers(16384, 32768, size=8, endpoint=True)
+    return make_decode_case(f"gqa-decode S8 L16K-32K bs32 Hq{8 * group} Hkv8 D128 bf16", L, 32, 8 * group, 8,
+                            128, torch.bfloat16, seed)
+
+
 def stress_decode(block_size: int = 16, dtype: torch.dtype = torch.bfloat16, seed: int = 5,
                   num_seqs: int = 256) -> PagedCase:
     """256 sequences, cached lengths log-uniform in [64, 8192], 32 q / 8 kv heads, D 128;
@@ -290,4 +300,5 @@ WORKLOADS = {
     "prefill_chunk": prefill_chunk,
     "stress_decode": stress_decode,
     "mixed_batch": mixed_batch,
+    "gqa_decode": gqa_decode,
 }
