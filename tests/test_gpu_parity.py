@@ -67,6 +67,17 @@ def test_decode_shape_sweep(oracle_mod, dtype, D, G, bs):
         assert mx < 1e-5
 
 
+@pytest.mark.parametrize("Hkv", [1, 4, 8, 16])
+@pytest.mark.parametrize("D", [64, 128])
+def test_decode_eight_query_heads_per_kv_head(oracle_mod, Hkv, D):
+    """Eight query heads per kv head run as two query slices of four heads per kv head: one
+    kv head (four token slices), one group of four, two and four groups (one token slice),
+    with a long sequence split over many CTAs."""
+    case = workloads.make_decode_case("g8", DECODE_LENS + [9000], 16, 8 * Hkv, Hkv, D, torch.bfloat16,
+                                      seed=800 + Hkv * 10 + D, free_frac=0.1)
+    check_case(case, oracle_mod)
+
+
 def test_decode_zero_context_gives_zero_row(oracle_mod):
     case = workloads.make_decode_case("zero", [40, 3, 700], 16, 8, 2, 128, torch.bfloat16, 9)
     case.context_lens[1] = 0       # sequence 1 attends nothing
