@@ -144,6 +144,12 @@ size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads, i
  *   out[s][h] = sum_j softmax_j(scale * q[s][h] . k_j) v_j over j < context_lens[s];
  *   a sequence with context length 0 gets an all-zero row.
  * Accumulation is fp32; the result does not depend on the split.
+ * With eight query heads per kv head, an fp16/bf16 cache and num_seqs * num_kv_heads
+ * >= 0.4 x the SM count, the rows run on the tensor cores instead (the chunked-prefill
+ * kernel with one-token chunks): q.k and p.v in fp32 accumulators, the softmax weights
+ * rounded to the cache's type before p.v (as in pa_prefill_chunk), each (sequence, kv
+ * head) in one fixed key order, so that a row does not depend on the rest of the batch;
+ * the workspace is then not touched.
  */
 int pa_decode(void *out, pa_dtype out_dtype, const void *query, const void *key_cache,
               const void *value_cache, const int32_t *block_tables, int max_blocks_per_seq,
@@ -172,7 +178,9 @@ int pa_decode(void *out, pa_dtype out_dtype, const void *query, const void *key_
  * equal those of pa_reshape_and_cache(key, value, ..., slot_mapping, num_seqs, ...) and
  * pa_decode(...) on the same stream, bit for bit.  Otherwise the pools are written as
  * stated and out is unspecified.  The launch that streams a sequence's last keys stores
- * the token and uses it from the same copy, so no kernel boundary separates the two.
+ * the token and uses it from the same copy, so no kernel boundary separates the two
+ * (where pa_decode runs its rows on the tensor cores, the write is a launch of its own
+ * in front of them).
  */
 int pa_decode_write(void *out, pa_dtype out_dtype, const void *query, const void *key,
                     const void *value, const int64_t *slot_mapping, void *key_cache,

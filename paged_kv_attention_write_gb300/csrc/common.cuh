@@ -232,6 +232,7 @@ struct PrefillArgs {
     pa_dtype kv_dtype;
     int32_t *status;
     cudaStream_t stream;
+    int decode_rows = 0;  // one query row per sequence (token s), no query_start_loc
 };
 
 int launch_reshape_and_cache(const void *key, const void *value, void *key_cache,

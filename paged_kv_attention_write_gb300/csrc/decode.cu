@@ -79,6 +79,29 @@ int launch_decode(const DecodeArgs &a) {
     const Layout L = layout(a.num_seqs, a.num_heads, a.num_kv_heads, a.head_dim,
                             sms < kMaxPieces ? sms : kMaxPieces);
     if (a.workspace_bytes < L.total) return PA_ERR_WORKSPACE;
+    // Eight query heads per kv head on a 16-bit cache, with (sequence, kv head) pairs enough
+    // to occupy most SMs: each sequence's query row goes through the tensor-core chunk kernel
+    // as a one-token chunk (q.k and p.v on the tensor cores, the weights rounded to the
+    // cache's type before p.v), which outruns the CUDA-core split for this grouping; a fused
+    // cache write becomes the cache-write launch in front of it.
+    const int G8 = a.num_heads / a.num_kv_heads;
+    if (G8 == 8 && a.kv_dtype != PA_F32 && !a.rope_freqs && 5 * (int64_t)a.num_seqs * a.num_kv_heads >= 2 * (int64_t)sms) {
+        if (a.new_key) {
+            const int eb16 = 2;
+            const int rc = launch_reshape_and_cache(a.new_key, a.new_value, const_cast<void *>(a.key_cache),
+                                                    const_cast<void *>(a.value_cache), a.slot_mapping, a.num_seqs,
+                                                    a.num_kv_heads * a.head_dim * eb16, a.block_size, a.num_blocks,
+                                                    a.status, a.stream);
+            if (rc != PA_OK) return rc;
+        }
+        PrefillArgs pf{a.out,          a.out_dtype,       a.query,        nullptr,      a.num_seqs,
+                       1,              a.key_cache,       a.value_cache,  a.block_tables, a.max_blocks_per_seq,
+                       a.context_lens, a.max_context_len, a.num_seqs,     a.num_heads,  a.num_kv_heads,
+                       a.head_dim,     a.block_size,      a.num_blocks,   a.scale,      a.kv_dtype,
+                       a.status,       a.stream};
+        pf.decode_rows = 1;
+        return launch_prefill(pf);
+    }
     char *ws = static_cast<char *>(a.workspace);
     DecodeParams prm{};
     prm.out = a.out;

@@ -206,6 +206,11 @@ struct PrefillParams {
     int32_t *status;
 };
 
+// The kernels' DR (decode rows) instantiations: sequence s has one query row, token s, at
+// position context_lens[s] - 1 (query_start_loc is not read); a sequence with nothing to
+// attend gets zero rows, and a negative or too long context is reported and clamped, as in
+// the decode kernels.  The other instantiations never see these branches.
+
 // ---------------------------------------------------------------- work items and their order
 // A unit is (sequence s, query tile qt), numbered s * q_tiles + qt; an item is (unit, kv
 // head).  Items are ranked unit-major: the units of rank r give items r*Hkv .. r*Hkv+Hkv-1.
@@ -220,9 +225,16 @@ __device__ __forceinline__ int64_t round_item(int k, int P, int c) {
 }
 
 // Key tiles the unit (s, qt) runs through; 0 for an empty or invalid unit.
+template <bool DR>
 __device__ __forceinline__ int unit_tiles(const PrefillParams &p, int s, int qt, int TT) {
-    const int q0 = p.query_start_loc[s];
-    const int Lq = p.query_start_loc[s + 1] - q0;
+    int q0, Lq;
+    if constexpr (DR) {
+        q0 = s;
+        Lq = 1;
+    } else {
+        q0 = p.query_start_loc[s];
+        Lq = p.query_start_loc[s + 1] - q0;
+    }
     if (q0 < 0 || Lq < 0 || (int64_t)q0 + Lq > p.num_tokens || qt * TT >= Lq) return 0;
     const int C = min(p.context_lens[s], min(p.max_blocks_per_seq * p.block_size, p.max_context_len));
     if (Lq > C) return 0;
@@ -233,6 +245,7 @@ __device__ __forceinline__ int unit_tiles(const PrefillParams &p, int s, int qt,
 // shared memory: every CTA computes the same order), and lists the unit of each of this
 // CTA's rounds in my_units.  Called by every thread; `scratch` is shared memory that
 // nothing else touches until the call returns.
+template <bool DR>
 __device__ void plan_units(const PrefillParams &p, int TT, int P, int c, unsigned char *scratch,
                            uint16_t *my_units) {
     const int Q = p.q_tiles, U = p.num_seqs * Q;
@@ -245,7 +258,7 @@ __device__ void plan_units(const PrefillParams &p, int TT, int P, int c, unsigne
     for (int i = tid; i < kPlanBins + kPlanBins / 32; i += NT) hist[i] = 0;
     __syncthreads();
     for (int u = tid; u < U; u += NT) {
-        const int w = min(unit_tiles(p, u / Q, u % Q, TT), kPlanBins - 1);
+        const int w = min(unit_tiles<DR>(p, u / Q, u % Q, TT), kPlanBins - 1);
         wt[u] = (uint16_t)w;
         atomicAdd(&hist[hslot(w)], 1);
     }
@@ -298,6 +311,7 @@ struct PfCursor {
     bool have;
     int unit, g, q0, q1, C;
 
+    template <bool DR>
     __device__ __forceinline__ void fetch(const PrefillParams &p, int k, bool planned,
                                           const uint16_t *my_units) {
         const int P = gridDim.x, c = blockIdx.x;
@@ -308,11 +322,17 @@ struct PfCursor {
         g = (int)(idx % p.num_kv_heads);
         unit = planned ? my_units[k] : (rank / Q) * Q + Q - 1 - rank % Q;
         const int s = unit / Q;
-        q0 = p.query_start_loc[s];
-        q1 = p.query_start_loc[s + 1];
+        if constexpr (DR) {
+            q0 = s;
+            q1 = s + 1;
+        } else {
+            q0 = p.query_start_loc[s];
+            q1 = p.query_start_loc[s + 1];
+        }
         C = p.context_lens[s];
     }
 
+    template <bool DR>
     __device__ __forceinline__ bool resolve(const PrefillParams &p, int TT, bool rep, PfItem &it) const {
         it.s = unit / p.q_tiles;
         it.qt = unit % p.q_tiles;
@@ -326,6 +346,13 @@ struct PfCursor {
         if (it.qt * TT >= it.Lq) return false;
         const int cap = min(p.max_blocks_per_seq * p.block_size, p.max_context_len);
         int Cc = C;
+        if constexpr (DR) {
+            if (Cc < 0 || Cc > cap) {
+                if (rep) report(p.status, PA_DEVERR_CONTEXT);
+                Cc = Cc < 0 ? 0 : cap;
+            }
+            if (Cc == 0) return false;  // a zero row, written at the start
+        }
         if (Cc > cap || it.Lq > Cc) {
             if (rep) report(p.status, Cc > cap ? PA_DEVERR_CONTEXT : PA_DEVERR_QUERY);
             if (Cc > cap) Cc = cap;
@@ -368,7 +395,7 @@ constexpr uint32_t kTmemCols = 512;
 constexpr int kSBufs = 3;
 constexpr uint32_t kTmemO = kSBufs * kBN;
 
-template <class T, int D, int G>
+template <class T, int D, int G, bool DR>
 __global__ void __launch_bounds__(kPfThreads, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                   const __grid_constant__ CUtensorMap vmap, const PrefillParams p) {
@@ -421,7 +448,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
 
     const int rounds = (p.num_items + gridDim.x - 1) / gridDim.x;
     const bool planned = p.num_seqs * p.q_tiles <= kPlanMaxUnits && rounds <= kMaxRounds;
-    if (planned) plan_units(p, TT, gridDim.x, blockIdx.x, smem + Sh::OFF_K, my_units);
+    if (planned) plan_units<DR>(p, TT, gridDim.x, blockIdx.x, smem + Sh::OFF_K, my_units);
 
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -456,11 +483,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
         const uint32_t box_bytes = (uint32_t)bs * 128 * Sh::HALVES;  // one block of one kv head
         bool ok = true;
         int t = 0, vi = 0;
-        cur.fetch(p, 0, planned, my_units);
+        cur.fetch<DR>(p, 0, planned, my_units);
         for (int k = 0; ok && cur.have; ++k) {
             PfItem it;
-            const bool live = cur.resolve(p, TT, false, it);
-            cur.fetch(p, k + 1, planned, my_units);
+            const bool live = cur.resolve<DR>(p, TT, false, it);
+            cur.fetch<DR>(p, k + 1, planned, my_units);
             if (!live) continue;
             const int32_t *bt = p.block_tables + (int64_t)it.s * p.max_blocks_per_seq;
             auto block_id = [&](int j) {
@@ -523,11 +550,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
         if (lane == 0) {
             bool ok = true;
             int t = 0, vi = 0;
-            cur.fetch(p, 0, planned, my_units);
+            cur.fetch<DR>(p, 0, planned, my_units);
             for (int k = 0; ok && cur.have; ++k) {
                 PfItem it;
-                const bool live = cur.resolve(p, TT, false, it);
-                cur.fetch(p, k + 1, planned, my_units);
+                const bool live = cur.resolve<DR>(p, TT, false, it);
+                cur.fetch<DR>(p, k + 1, planned, my_units);
                 if (!live) continue;
                 const int qb = vi % NQ;
                 ok = !*abort_v && mbar_wait(bar(BQF + qb), (vi / NQ) & 1, p.status);
@@ -559,11 +586,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
         if (lane == 0) {
             bool ok = true;
             int t = 0;
-            cur.fetch(p, 0, planned, my_units);
+            cur.fetch<DR>(p, 0, planned, my_units);
             for (int k = 0; ok && cur.have; ++k) {
                 PfItem it;
-                const bool live = cur.resolve(p, TT, false, it);
-                cur.fetch(p, k + 1, planned, my_units);
+                const bool live = cur.resolve<DR>(p, TT, false, it);
+                cur.fetch<DR>(p, k + 1, planned, my_units);
                 if (!live) continue;
                 for (int j = 0; j < it.n_tiles && ok; ++j, ++t) {
                     const int pb = t % kSBufs, st = t % NV;
@@ -604,11 +631,20 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
         const float sc = p.qk_scale_log2;
         bool ok = true;
         int t = 0;
-        cur.fetch(p, 0, planned, my_units);
+        if constexpr (DR) {  // zero rows for the sequences with nothing to attend
+            const int cap = min(p.max_blocks_per_seq * p.block_size, p.max_context_len);
+            const int words = p.num_heads * D * (p.out_dtype == PA_F32 ? 4 : 2) / 4;
+            for (int s = blockIdx.x; s < p.num_seqs; s += gridDim.x) {
+                if (min(p.context_lens[s], cap) > 0) continue;
+                uint32_t *row = static_cast<uint32_t *>(p.out) + (int64_t)s * words;
+                for (int i = sidx; i < words; i += 256) row[i] = 0u;
+            }
+        }
+        cur.fetch<DR>(p, 0, planned, my_units);
         for (int k = 0; ok && cur.have; ++k) {
             PfItem it;
-            const bool live = cur.resolve(p, TT, warp == 4 && lane == 0, it);
-            cur.fetch(p, k + 1, planned, my_units);
+            const bool live = cur.resolve<DR>(p, TT, warp == 4 && lane == 0, it);
+            cur.fetch<DR>(p, k + 1, planned, my_units);
             if (!live) continue;
             // rows past the chunk (a ragged last tile) are computed but never stored; they
             // see exactly the keys that were loaded
@@ -819,7 +855,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
     }
 }
 
-template <class T, int D, int G>
+template <class T, int D, int G, bool DR = false>
 int launch_typed(const PrefillParams &prm, const CUtensorMap &qm, const CUtensorMap &km,
                  const CUtensorMap &vm, int max_query_len, int num_seqs, cudaStream_t st) {
     constexpr int TT = kBM / G;
@@ -833,15 +869,17 @@ int launch_typed(const PrefillParams &prm, const CUtensorMap &qm, const CUtensor
     // one persistent CTA per SM (the shared memory allows one)
     const int sms = device_sm_count();
     const int grid = (int)std::min<int64_t>(items, sms > 0 ? sms : 1);
-    return launch_pdl_smem(prefill_tc_kernel<T, D, G>, smem_ready, dim3(grid), dim3(kPfThreads), smem, st, qm,
+    return launch_pdl_smem(prefill_tc_kernel<T, D, G, DR>, smem_ready, dim3(grid), dim3(kPfThreads), smem, st, qm,
                            km, vm, p) == cudaSuccess
                ? PA_OK
                : PA_ERR_CUDA;
 }
 
 template <class T, int D>
-int dispatch_g(const PrefillParams &prm, int G, const CUtensorMap &qm, const CUtensorMap &km,
+int dispatch_g(const PrefillParams &prm, int G, bool decode_rows, const CUtensorMap &qm, const CUtensorMap &km,
                const CUtensorMap &vm, int mq, int S, cudaStream_t st) {
+    if (decode_rows)  // built for eight query heads per kv head, the grouping that routes here
+        return G == 8 ? launch_typed<T, D, 8, true>(prm, qm, km, vm, mq, S, st) : PA_ERR_UNSUPPORTED;
     switch (G) {
         case 1: return launch_typed<T, D, 1>(prm, qm, km, vm, mq, S, st);
         case 2: return launch_typed<T, D, 2>(prm, qm, km, vm, mq, S, st);
@@ -852,11 +890,11 @@ int dispatch_g(const PrefillParams &prm, int G, const CUtensorMap &qm, const CUt
 }
 
 template <class T>
-int dispatch_d(const PrefillParams &prm, int D, int G, const CUtensorMap &qm, const CUtensorMap &km,
+int dispatch_d(const PrefillParams &prm, int D, int G, bool dr, const CUtensorMap &qm, const CUtensorMap &km,
                const CUtensorMap &vm, int mq, int S, cudaStream_t st) {
     switch (D) {
-        case 64: return dispatch_g<T, 64>(prm, G, qm, km, vm, mq, S, st);
-        case 128: return dispatch_g<T, 128>(prm, G, qm, km, vm, mq, S, st);
+        case 64: return dispatch_g<T, 64>(prm, G, dr, qm, km, vm, mq, S, st);
+        case 128: return dispatch_g<T, 128>(prm, G, dr, qm, km, vm, mq, S, st);
         default: return PA_ERR_UNSUPPORTED;
     }
 }
@@ -896,8 +934,12 @@ int launch_prefill(const PrefillArgs &a) {
             PA_OK)
         return PA_ERR_CUDA;
     switch (a.kv_dtype) {
-        case PA_F16: return dispatch_d<F16>(prm, a.head_dim, G, qm, km, vm, a.max_query_len, a.num_seqs, a.stream);
-        case PA_BF16: return dispatch_d<BF16>(prm, a.head_dim, G, qm, km, vm, a.max_query_len, a.num_seqs, a.stream);
+        case PA_F16:
+            return dispatch_d<F16>(prm, a.head_dim, G, a.decode_rows != 0, qm, km, vm, a.max_query_len, a.num_seqs,
+                                   a.stream);
+        case PA_BF16:
+            return dispatch_d<BF16>(prm, a.head_dim, G, a.decode_rows != 0, qm, km, vm, a.max_query_len, a.num_seqs,
+                                    a.stream);
         default: return PA_ERR_UNSUPPORTED;
     }
 }
