@@ -148,8 +148,10 @@ size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads, i
  * >= 0.4 x the SM count, the rows run on the tensor cores instead (the chunked-prefill
  * kernel with one-token chunks): q.k and p.v in fp32 accumulators, the softmax weights
  * rounded to the cache's type before p.v (as in pa_prefill_chunk), each (sequence, kv
- * head) in one fixed key order, so that a row does not depend on the rest of the batch;
- * the workspace is then not touched.
+ * head) in one fixed key order, so that a row does not depend on the rest of the batch
+ * while the call stays on this path; the workspace is then not touched.  A row computed
+ * on the two paths (a small batch and a large one) agrees within the attention tolerance,
+ * not bit for bit.  One to four query heads per kv head always take the split path.
  */
 int pa_decode(void *out, pa_dtype out_dtype, const void *query, const void *key_cache,
               const void *value_cache, const int32_t *block_tables, int max_blocks_per_seq,
